@@ -1,0 +1,36 @@
+"""Plain fp64 CPU oracle for packed variable-length context-parallel attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import or run this package.
+The library under ``context_attention_cpattn_gb300`` never imports it, and it
+imports nothing from the library: the two share no code.  The only common
+dependency is the seeded input module ``inputs``, which holds no arithmetic of
+the method.
+
+Contents and the passages each follows:
+
+* ``attention`` - softmax attention inside each packed sequence, written out
+  from its definition (THD packing with cu_seqlens: "Speeding up
+  Variable-Length Training with Dynamic Context Parallelism and NVIDIA
+  Megatron Core", section on dynamic rescheduling and packing, Fig. 1; the
+  result must not depend on how the sequence is split: "Scaling video
+  training with parallelism", opening section).  Also the attention of a
+  query-row set over a key-row set (one ring step's block, "Scaling video
+  training with parallelism", section 2, Ring Attention).
+* ``merge`` - the exact log-sum-exp merge of block partials.  The pages name
+  blockwise attention with a KV ring but not the merge; the merge written
+  here is the plain identity that recombines softmax partials exactly.
+* ``plan`` - zigzag, 2-D h x w and contiguous context-parallel splits and the
+  ring schedule (LongVILA news article, Fig. 5 / Table 2 ZIGZAG-RINGATTN;
+  LongCat-Video context-parallel article, tensor split strategy and its FAQ;
+  "Scaling video training with parallelism", section 3, Fig. 2).
+* ``loss`` - per-token loss normalisation over valid tokens (Dynamic-CP
+  article, section "Loss computation and FLOPS statistics").
+* ``flops`` - THD-aware FLOP count from real sequence lengths (same section).
+
+Every function here is pinned by ``tests/test_oracle_*.py`` against brute
+force, closed forms, library routines and invariants; no function is
+"parity unpinned".
+"""
+
+from . import attention, flops, loss, merge, plan  # noqa: F401

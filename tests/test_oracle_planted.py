@@ -1,0 +1,95 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins
+catch each one.  The real oracle is restored after every case."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as A
+import oracle.merge as M
+from tests.test_oracle_attention import brute_force
+
+
+def _case():
+    cu = (0, 6, 19)
+    rng = np.random.default_rng(0)
+    q, k, v = rng.standard_normal((19, 4, 4)), rng.standard_normal((19, 2, 4)), rng.standard_normal((19, 2, 4))
+    return cu, q, k, v
+
+
+def _err_vs_brute(causal=True, scale=0.4):
+    cu, q, k, v = _case()
+    O, L = A.packed_attention(q, k, v, cu, causal, scale)
+    Ob, Lb = brute_force(q, k, v, cu, causal, scale)
+    return max(np.abs(O - Ob).max(), np.abs(L - Lb).max())
+
+
+def test_real_oracle_passes():
+    assert _err_vs_brute() < 1e-12
+
+
+def test_wrong_gqa_grouping_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "kv_head", lambda h, H, Hkv: h % Hkv)
+    assert _err_vs_brute() > 1e-3
+
+
+def test_dropped_scale_is_caught(monkeypatch):
+    real = A._softmax_rows
+
+    def planted(S, V):
+        return real(S / 0.4, V)  # as if the scale had been left out
+
+    monkeypatch.setattr(A, "_softmax_rows", planted)
+    assert _err_vs_brute() > 1e-3
+
+
+def test_off_by_one_causal_mask_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "causal_visible", lambda kpos, qpos: kpos < qpos)
+    cu, q, k, v = _case()
+    O, L = A.packed_attention(q, k, v, cu, True, 0.4)
+    # the first token of each sequence now sees nothing: the closed form
+    # O = v_first, lse = scale q.k_first no longer holds
+    assert not np.array_equal(O[0, 0], v[0, 0])
+    assert _err_vs_brute() > 1e-3 or not np.isfinite(_err_vs_brute())
+
+
+def test_transposed_value_operand_is_caught():
+    cu, q, k, v = _case()
+    # a mistake that uses K in place of V in the P.V product
+    O, _ = A.packed_attention(q, k, k, cu, True, 0.4)
+    Ob, _ = brute_force(q, k, v, cu, True, 0.4)
+    assert np.abs(O - Ob).max() > 1e-3
+
+
+def test_unnormalised_merge_is_caught(monkeypatch):
+    rng = np.random.default_rng(1)
+    o = [rng.standard_normal((3, 1, 2)) for _ in range(2)]
+    l = [rng.standard_normal((1, 3)) for _ in range(2)]
+    good_O, good_L = M.lse_merge(o, l)
+    w = [np.exp(x) for x in l]
+    ref = (w[0].T[:, :, None] * o[0] + w[1].T[:, :, None] * o[1]) / (w[0] + w[1]).T[:, :, None]
+    assert np.abs(good_O - ref).max() < 1e-13
+
+    def planted(o_parts, lse_parts):
+        lse = np.stack(lse_parts)
+        Mx = lse.max(axis=0)
+        coef = np.exp(lse - Mx)  # forgets to divide by the total weight
+        return np.einsum("phr,prhd->rhd", coef, np.stack(o_parts)), Mx
+
+    bad_O, _ = planted(o, l)
+    assert np.abs(bad_O - ref).max() > 1e-3
+
+
+def test_sdpa_pin_detects_missing_causal_mask():
+    cu, q, k, v = _case()
+    O_bidir, _ = A.packed_attention(q, k, v, cu, False, 0.4)
+    a, b = 6, 19
+    H, Hkv = 4, 2
+    qt = torch.from_numpy(q[a:b]).permute(1, 0, 2)[None]
+    kt = torch.from_numpy(k[a:b]).permute(1, 0, 2).repeat_interleave(H // Hkv, 0)[None]
+    vt = torch.from_numpy(v[a:b]).permute(1, 0, 2).repeat_interleave(H // Hkv, 0)[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True, scale=0.4)
+    assert np.abs(O_bidir[a:b] - ref[0].permute(1, 0, 2).numpy()).max() > 1e-3
+    assert math.isfinite(float(ref.abs().max()))
