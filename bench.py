@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Packed variable-length context-parallel attention forward: throughput on GB300.
+
+Metric: packed varlen attention fwd TFLOP/s over valid tokens (THD-aware FLOPs
+4*D*H*sum pairs(L), counted from real sequence lengths) and the fraction of
+the measured dense BF16 tensor peak.
+
+A step is one pass of the hot path over one synthetic micro-batch already
+resident in HBM: the whole packed forward (every virtual rank's ring steps
+with the exact LSE merge fused in, one launch) plus the per-token loss
+normalisation.  The context-parallel plan is built once per micro-batch
+layout on the host, outside the timed region, as the pages' Dynamic-CP
+scheduler also plans asynchronously off the critical path; its host time is
+reported as plan_ms.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 oracle on host cores
+
+Under torchrun (N>1) every rank runs an independent replica of the workload
+on its own GPU (no data-path collective); a barrier and a max over ranks
+bracket the timed region.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+# Host-only legs pin BLAS to one thread per worker before numpy loads.
+if "--cpu-baseline-child" in sys.argv or ("--impl" in sys.argv and "reference" in sys.argv):
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
+import numpy as np  # noqa: E402
+
+METRIC = "packed varlen attention fwd TFLOP/s (valid tokens) and % of GB300 BF16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "dynamic_cp_microbatch"
+FALLBACK_BF16_TFLOPS = 1900.0
+TC_SOURCES = ("context_attention_cpattn_gb300/csrc/attn_tc.cu", "context_attention_cpattn_gb300/csrc/common.cuh")
+TRAFFIC_FILE = "profiles/attn_fwd_tc_dynamic_cp_microbatch.md"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--rows", type=int, default=0, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ replicas
+
+class Replicas:
+    """Rank bookkeeping for N independent replicas: a barrier and a max over
+    ranks around the timed region, nothing in the data path."""
+
+    def __init__(self, backend: str | None = None):
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local = int(os.environ.get("LOCAL_RANK", str(self.rank)))
+        self.backend = backend
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend or "nccl")
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.dist is None:
+            return x
+        import torch
+        dev = f"cuda:{self.local}" if self.backend in (None, "nccl") else "cpu"
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    def __init__(self, gpu_index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(gpu_index)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        return summarise_clocks(open(self.path).read())
+
+
+def summarise_clocks(text: str) -> dict | None:
+    sm, mx, reasons = [], [], set()
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    for line in text.strip().splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    top = max(sm)
+    loaded = [s for s in sm if s >= 0.5 * top] or sm
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "samples": len(sm),
+            "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ peaks, traffic
+
+def measured_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "of measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "of fallback"
+
+
+def tc_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in TC_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source and this workload."""
+    path = os.path.join(ROOT, TRAFFIC_FILE)
+    if workload != DEFAULT_WORKLOAD or not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if line.startswith("traffic_bytes_per_launch=") or line.startswith("source_sha256="):
+            k, v = line.strip().split("=", 1)
+            vals[k] = v
+    if vals.get("source_sha256") != tc_source_hash() or "traffic_bytes_per_launch" not in vals:
+        return None
+    return float(vals["traffic_bytes_per_launch"])
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+def row_flops(cu, rows, H, D, causal) -> int:
+    cu = np.asarray(cu, dtype=np.int64)
+    seq = np.searchsorted(cu, rows, side="right") - 1
+    vis = (rows - cu[seq] + 1) if causal else (cu[seq + 1] - cu[seq])
+    return int(4 * D * H * int(vis.sum()))
+
+
+def oracle_rows(w, rows, q, k, v, threads):
+    from oracle import attention as A
+    t0 = time.perf_counter()
+    A.attention_at_rows(q, k, v, w.cu_seqlens, rows, w.causal, w.scale, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_child(args):
+    """Runs in a subprocess with single-threaded BLAS: the oracle on sampled
+    query rows (all heads) of the workload, on every host core."""
+    import inputs
+    w = inputs.workload(args.workload)
+    q, k, v = inputs.make_qkv(w)
+    cores = host_cores()
+    rows = inputs.sample_rows(w.T, max(8, args.rows or 64), seed=w.seed + 1)
+    dt = oracle_rows(w, rows, q, k, v, cores)
+    if not args.rows:  # size the measured sample to the target duration
+        n = int(min(w.T, max(64, len(rows) * args.cpu_seconds / max(dt, 1e-3))))
+        rows = inputs.sample_rows(w.T, n, seed=w.seed + 2)
+        dt = oracle_rows(w, rows, q, k, v, cores)
+    fl = row_flops(w.cu_seqlens, rows, w.H, w.D, w.causal)
+    print(json.dumps({"value": fl / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+                      "sample": f"{len(rows)} seeded query rows x {w.H} heads of {w.name} "
+                                f"({fl:.3e} FLOPs, {dt:.2f} s, fp64 numpy, {cores} threads)"}))
+
+
+def run_cpu_baseline(args) -> dict | None:
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = "1"
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", args.workload,
+           "--cpu-seconds", str(args.cpu_seconds)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as ex:  # noqa: BLE001
+        return {"value": None, "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": f"failed: {ex}"}
+
+
+def config_of(w, flops):
+    cfg = {"workload": w.name, "T": w.T, "n_seqs": w.n_seqs, "H": w.H, "Hkv": w.Hkv, "D": w.D, "causal": w.causal,
+           "mode": w.mode, "cp": w.cp, "flops_per_step": flops, "seed": w.seed}
+    if w.grid:
+        cfg["grid"] = list(w.grid)
+    in_bytes = w.T * (w.H + 2 * w.Hkv) * w.D * (2 if w.dtype == "bf16" else 4)
+    cfg["l2"] = f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB read per step)"
+    return cfg
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores, as the reference arm."""
+    import inputs
+    from oracle import flops as OF
+    w = inputs.workload(args.workload)
+    q, k, v = inputs.make_qkv(w)
+    cores = host_cores()
+    rows_per_step = args.rows or 96
+    times, fl_total = [], 0
+    for i in range(args.warmup + args.steps):
+        rows = inputs.sample_rows(w.T, rows_per_step, seed=w.seed + 100 + i)
+        dt = oracle_rows(w, rows, q, k, v, cores)
+        if i >= args.warmup:
+            times.append(dt)
+            fl_total += row_flops(w.cu_seqlens, rows, w.H, w.D, w.causal)
+    total = sum(times)
+    value = fl_total / total / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, OF.fwd_flops(w.cu_seqlens, w.H, w.D, w.causal)),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step {rows_per_step} seeded query rows x {w.H} heads of {w.name}, "
+                                       f"fp64 numpy on {cores} threads"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rep: Replicas):
+    import torch
+
+    import context_attention_cpattn_gb300 as cp
+    import inputs
+
+    torch.cuda.set_device(rep.local)
+    dev = torch.device("cuda", rep.local)
+    w = inputs.workload(args.workload)
+    q_h, k_h, v_h = inputs.make_qkv(w, pin=True)
+    loss_h, valid_h = inputs.make_loss_inputs(w)
+    loss_h, valid_h = loss_h.pin_memory(), valid_h.pin_memory()
+    qd, kd, vd = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    loss_d, valid_d = loss_h.to(dev), valid_h.to(dev)
+
+    t0 = time.perf_counter()
+    plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
+    ws_bytes = cp.cpattn_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal)
+    plan_ms = 1e3 * (time.perf_counter() - t0)
+    flops = cp.cpattn_fwd_flops(w.cu_seqlens, w.H, w.D, w.causal)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.H, w.T), dtype=torch.float32, device=dev)
+    out_loss = torch.empty(1, dtype=torch.float64, device=dev)
+    out_cnt = torch.empty(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 2 + (3 if w.mode == "grid2d" else 0)
+
+    def step(ev0=None, ev1=None):
+        if ev0 is not None:
+            ev0.record(stream)
+        cp.cpattn_fwd(plan, qd, kd, vd, o, lse, ws, scale=w.scale, causal=w.causal, stream=stream)
+        if ev1 is not None:
+            ev1.record(stream)
+        cp.cpattn_token_loss_norm(loss_d, valid_d, out_loss, out_cnt, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    cp.cpattn_sync_status(ws, stream)
+
+    sampler = ClockSampler(rep.local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rep.rank}.csv")
+                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/cpattn_clocks_{rep.rank}.csv")
+    fwd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rep.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        step(*fwd_ev[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    rep.barrier()
+    clocks = sampler.stop()
+    cp.cpattn_sync_status(ws, stream)
+    elapsed = start.elapsed_time(end) / 1e3
+    fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
+    elapsed_max = rep.max(elapsed)
+    value = rep.world * args.steps * flops / elapsed_max / 1e12
+
+    # end to end through the public API: inputs from pinned host memory, result read back
+    e2e = None
+    if not args.no_e2e:
+        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        res_h = torch.empty(2, dtype=torch.float64, pin_memory=True)
+        res_d = torch.empty(2, dtype=torch.float64, device=dev)
+
+        def e2e_step():
+            qd.copy_(q_h, non_blocking=True)
+            kd.copy_(k_h, non_blocking=True)
+            vd.copy_(v_h, non_blocking=True)
+            loss_d.copy_(loss_h, non_blocking=True)
+            valid_d.copy_(valid_h, non_blocking=True)
+            step()
+            res_d[0:1].copy_(out_loss)
+            res_d[1:2].copy_(out_cnt.to(torch.float64))
+            o_h.copy_(o, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+            res_h.copy_(res_d, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        rep.barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        rep.barrier()
+        e2e_s = rep.max(e0.elapsed_time(e1) / 1e3)
+        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, loss_h, valid_h))
+        d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * lse_h.element_size() + res_h.numel() * 8
+        e2e = {"value": rep.world * args.steps * flops / e2e_s / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        cp.cpattn_sync_status(ws, stream)
+
+    if rep.rank != 0:
+        return
+    peak, peak_src = measured_peak()
+    fwd_mean_s = statistics.fmean(fwd_ms) / 1e3
+    achieved = flops / fwd_mean_s / 1e12
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": rep.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * elapsed_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_of(w, flops),
+        "pct_of_bf16_peak": 100.0 * value / (peak * rep.world),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "peak_source": peak_src, "traffic": traffic,
+                     "kernel": "attn_fwd_tc_kernel (cpattn_fwd, CUDA events per call)"},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "plan_ms": plan_ms,
+        "fwd_ms_mean": 1e3 * fwd_mean_s,
+        "fwd_ms_min": min(fwd_ms),
+        "tc_source_sha256": tc_source_hash(),
+    }
+    if not args.no_cpu_baseline and rep.world == 1:
+        line["cpu_baseline"] = run_cpu_baseline(args)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.cpu_baseline_child:
+        cpu_baseline_child(args)
+        return
+    if args.impl == "reference":
+        # host-only: rank 0 runs it, other ranks exit without work (no process group)
+        if int(os.environ.get("RANK", "0")) == 0:
+            run_reference(args)
+        return
+    rep = Replicas()
+    try:
+        run_ours(args, rep)
+    finally:
+        rep.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,275 @@
+"""cpattn - packed variable-length context-parallel attention on one GB300.
+
+Thin Python binding of ``libcpattn.so`` (C ABI in ``include/cpattn.h``).  The
+functions keep the C names and only marshal arguments: torch tensors are
+passed as device pointers and the current CUDA stream as the stream handle.
+Every step of the computation runs in the library's CUDA kernels; there is no
+Python or CPU fallback, and a missing library raises ``ImportError``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+from typing import Optional, Sequence
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libcpattn.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "cpattn.h")
+
+OK, INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA_ERROR, DEVICE_FAULT = range(6)
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA_ERROR", 5: "DEVICE_FAULT"}
+MODES = {"zigzag": 0, "grid2d": 1, "contiguous": 2}
+DTYPE_FP32, DTYPE_BF16 = 0, 1
+MASK_SKIP, MASK_FULL, MASK_DIAG, MASK_KV_HEAD, MASK_Q_TAIL = range(5)
+
+
+class CpattnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class _Grid(ctypes.Structure):
+    _fields_ = [("frames", ctypes.c_int32), ("height", ctypes.c_int32), ("width", ctypes.c_int32)]
+
+
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [("total_tokens", ctypes.c_int64), ("n_chunks", ctypes.c_int64), ("max_rank_tokens", ctypes.c_int64),
+                ("n_seqs", ctypes.c_int32), ("cp_size", ctypes.c_int32), ("mode", ctypes.c_int32),
+                ("split_h", ctypes.c_int32), ("split_w", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+_P, _I32, _I64, _SZ, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+
+_SIGNATURES = {
+    "cpattn_plan": [_P, _I32, _I32, _I32, _P, _P],
+    "cpattn_plan_destroy": [_P],
+    "cpattn_plan_get_info": [_P, _P],
+    "cpattn_plan_get_chunk_offsets": [_P, _P, _I64],
+    "cpattn_plan_get_chunk_ranks": [_P, _P, _I64],
+    "cpattn_plan_get_rank_offsets": [_P, _P, _I64],
+    "cpattn_plan_get_local_cu_seqlens": [_P, _I32, _P, _I64],
+    "cpattn_plan_get_index_map": [_P, _P, _I64],
+    "cpattn_plan_get_ring_schedule": [_P, _I32, _P, _P, _I64],
+    "cpattn_workspace_size": [_P, _I32, _I32, _I32, _I32, _I32, _P],
+    "cpattn_fwd": [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _I32, _P, _P, _P, _SZ, _P],
+    "cpattn_block_fwd": [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P],
+    "cpattn_merge": [_I32, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _I32, _P, _P],
+    "cpattn_gather_rows": [_P, _I64, _P, _P, _I64, _I64, _P],
+    "cpattn_scatter_rows": [_P, _P, _I64, _P, _I64, _I64, _P],
+    "cpattn_token_loss_norm": [_P, _P, _I64, _P, _P, _P, _P],
+    "cpattn_fwd_flops": [_P, _I32, _I32, _I32, _I32, _P, _P],
+    "cpattn_sync_status": [_P, _P],
+    "cpattn_last_error_string": [],
+    "cpattn_version": [],
+}
+
+
+def build(force: bool = False) -> str:
+    """Compile libcpattn.so for sm_103a in-tree (nvcc)."""
+    from ._build import build as _build
+    return _build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises ImportError if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with context_attention_cpattn_gb300.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_char_p if name in ("cpattn_last_error_string", "cpattn_version") else ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def header_functions() -> list:
+    """Names of every function declared in include/cpattn.h."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cpattn_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status: int):
+    if status != OK:
+        msg = lib().cpattn_last_error_string().decode()
+        raise CpattnError(status, msg)
+
+
+def version() -> str:
+    return lib().cpattn_version().decode()
+
+
+# ------------------------------------------------------------------ plans
+
+class Plan:
+    """A context-parallel split (library-owned host object)."""
+
+    def __init__(self, handle, cu_seqlens, cp, mode, grid):
+        self._h = handle
+        self.cu_seqlens = np.asarray(cu_seqlens, dtype=np.int32)
+        self.cp = cp
+        self.mode = mode
+        self.grid = grid
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h and _lib is not None:
+            _lib.cpattn_plan_destroy(h)
+            self._h = None
+
+    def info(self) -> dict:
+        out = _PlanInfo()
+        _check(lib().cpattn_plan_get_info(self._h, ctypes.byref(out)))
+        return {f: getattr(out, f) for f, _ in _PlanInfo._fields_ if f != "reserved"}
+
+    def _get(self, fn, n, dtype, *pre):
+        out = np.empty(n, dtype=dtype)
+        _check(getattr(lib(), fn)(self._h, *pre, out.ctypes.data, n))
+        return out
+
+    def chunk_offsets(self):
+        return self._get("cpattn_plan_get_chunk_offsets", self.info()["n_chunks"] + 1, np.int64)
+
+    def chunk_ranks(self):
+        return self._get("cpattn_plan_get_chunk_ranks", self.info()["n_chunks"], np.int32)
+
+    def rank_offsets(self):
+        return self._get("cpattn_plan_get_rank_offsets", self.cp + 1, np.int64)
+
+    def local_cu_seqlens(self, rank: int):
+        return self._get("cpattn_plan_get_local_cu_seqlens", len(self.cu_seqlens), np.int32, rank)
+
+    def index_map(self):
+        return self._get("cpattn_plan_get_index_map", int(self.cu_seqlens[-1]), np.int64)
+
+    def ring_schedule(self, causal: bool):
+        n = self.cp * self.cp
+        kv = np.empty(n, dtype=np.int32)
+        kind = np.empty(n, dtype=np.int32)
+        _check(lib().cpattn_plan_get_ring_schedule(self._h, int(bool(causal)), kv.ctypes.data, kind.ctypes.data, n))
+        return kv.reshape(self.cp, self.cp), kind.reshape(self.cp, self.cp)
+
+
+def cpattn_plan(cu_seqlens, cp_size: int, mode="zigzag", grid=None) -> Plan:
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    m = MODES[mode] if isinstance(mode, str) else int(mode)
+    g = _Grid(*grid) if grid is not None else None
+    h = ctypes.c_void_p()
+    _check(lib().cpattn_plan(cu.ctypes.data, len(cu) - 1, int(cp_size), m,
+                             ctypes.byref(g) if g is not None else None, ctypes.byref(h)))
+    return Plan(h.value, cu, int(cp_size), m, grid)
+
+
+# ------------------------------------------------------------------ attention
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_FP32
+    raise CpattnError(UNSUPPORTED, f"dtype {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def cpattn_workspace_size(plan: Plan, H: int, Hkv: int, D: int, dtype, causal: bool) -> int:
+    code = dtype if isinstance(dtype, int) else _dtype_code_of(dtype)
+    out = ctypes.c_size_t()
+    _check(lib().cpattn_workspace_size(plan.handle, H, Hkv, D, code, int(bool(causal)), ctypes.byref(out)))
+    return out.value
+
+
+def _dtype_code_of(dtype) -> int:
+    import torch
+    return {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_FP32, "bf16": DTYPE_BF16, "fp32": DTYPE_FP32}[dtype]
+
+
+def cpattn_fwd(plan: Plan, q, k, v, o, lse, workspace, scale: Optional[float] = None, causal: bool = True,
+               stream=None):
+    """Whole packed forward.  q [T,H,D], k/v [T,Hkv,D], o [T,H,D], lse fp32 [H,T],
+    workspace a uint8 device tensor of at least cpattn_workspace_size bytes."""
+    T, H, D = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    _check(lib().cpattn_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), H, Hkv, D, scale,
+                            int(bool(causal)), _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
+                            _stream(stream)))
+
+
+def cpattn_block_fwd(plan: Plan, q, k, v, o_partial, lse_partial, workspace, q_rank: int, ring_step: int,
+                     scale: Optional[float] = None, causal: bool = True, stream=None):
+    """One ring step of one virtual rank: fp32 partial O [T_r,H,D] and LSE [H,T_r]."""
+    T, H, D = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    _check(lib().cpattn_block_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), H, Hkv, D, scale,
+                                  int(bool(causal)), int(q_rank), int(ring_step), _ptr(o_partial),
+                                  _ptr(lse_partial), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def cpattn_merge(o_parts: Sequence, lse_parts: Sequence, o_out, lse_out, out_rows=None, stream=None):
+    """Exact LSE merge of fp32 partials o_parts[i] [rows,H,D], lse_parts[i] [H,rows]
+    into o_out [out_rows_total,H,D] (fp32 or bf16) and lse_out [H,out_rows_total]."""
+    n = len(o_parts)
+    rows, H, D = o_parts[0].shape
+    op = (ctypes.c_void_p * n)(*[t.data_ptr() for t in o_parts])
+    lp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in lse_parts])
+    _check(lib().cpattn_merge(n, op, lp, rows, H, D, _ptr(out_rows), o_out.shape[0], _ptr(o_out),
+                              _dtype_code(o_out), _ptr(lse_out), _stream(stream)))
+
+
+def cpattn_gather_rows(src, dst, index, stream=None):
+    """dst[i] = src[index[i]] (rows of equal byte size)."""
+    row_bytes = dst[0].numel() * dst.element_size() if dst.shape[0] else 16
+    _check(lib().cpattn_gather_rows(_ptr(src), src.shape[0], _ptr(dst), _ptr(index), index.numel(), row_bytes,
+                                    _stream(stream)))
+
+
+def cpattn_scatter_rows(src, dst, index, stream=None):
+    """dst[index[i]] = src[i] (rows of equal byte size)."""
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else 16
+    _check(lib().cpattn_scatter_rows(_ptr(src), _ptr(dst), dst.shape[0], _ptr(index), index.numel(), row_bytes,
+                                     _stream(stream)))
+
+
+def cpattn_token_loss_norm(loss, valid, out_loss, out_count, out_loss_f32=None, stream=None):
+    """out_loss (fp64 [1]) = mean of loss over valid tokens; out_count (int64 [1]) = valid tokens."""
+    _check(lib().cpattn_token_loss_norm(_ptr(loss), _ptr(valid), loss.numel(), _ptr(out_loss), _ptr(out_count),
+                                        _ptr(out_loss_f32), _stream(stream)))
+
+
+def cpattn_fwd_flops(cu_seqlens, H: int, D: int, causal: bool) -> int:
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    out = ctypes.c_uint64()
+    _check(lib().cpattn_fwd_flops(cu.ctypes.data, len(cu) - 1, H, D, int(bool(causal)), ctypes.byref(out), None))
+    return int(out.value)
+
+
+def cpattn_sync_status(workspace=None, stream=None):
+    _check(lib().cpattn_sync_status(_ptr(workspace), _stream(stream)))

@@ -1,0 +1,484 @@
+// C ABI of libcpattn: argument checks, workspace layout and launches.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/cpattn.h"
+#include "kernels.hpp"
+#include "plan.hpp"
+
+using cpattn::KvRun;
+using cpattn::QTile;
+using cpattn::WorkList;
+using cpattn::WsHeader;
+
+namespace {
+
+thread_local std::string g_err;
+
+cpattn_status_t fail(cpattn_status_t s, const std::string& msg) {
+  g_err = msg;
+  return s;
+}
+
+cpattn_status_t cuda_fail(cudaError_t e, const char* what) {
+  g_err = std::string(what) + ": " + cudaGetErrorString(e);
+  return CPATTN_CUDA_ERROR;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+struct WsLayout {
+  size_t tiles = 0, runs = 0, idx = 0, q = 0, k = 0, v = 0, total = 0;
+};
+
+size_t elem_size(cpattn_dtype_t dt) { return dt == CPATTN_DTYPE_BF16 ? 2 : 4; }
+
+// header | tiles | runs | (GRID2D: index map | Q shards | K shards | V shards)
+WsLayout ws_layout(const cpattn_plan_t& p, const WorkList& wl, int H, int Hkv, int D, size_t es) {
+  WsLayout L;
+  size_t off = CPATTN_WS_HEADER_BYTES;
+  L.tiles = off;
+  off += align256(wl.tiles.size() * sizeof(QTile));
+  L.runs = off;
+  off += align256(wl.runs.size() * sizeof(KvRun));
+  if (p.mode == CPATTN_MODE_GRID2D) {
+    L.idx = off;
+    off += align256((size_t)p.T * sizeof(int64_t));
+    L.q = off;
+    off += align256((size_t)p.T * H * D * es);
+    L.k = off;
+    off += align256((size_t)p.T * Hkv * D * es);
+    L.v = off;
+    off += align256((size_t)p.T * Hkv * D * es);
+  }
+  L.total = off;
+  return L;
+}
+
+cpattn_status_t check_shape(int H, int Hkv, int D, cpattn_dtype_t dt) {
+  if (dt != CPATTN_DTYPE_FP32 && dt != CPATTN_DTYPE_BF16) return fail(CPATTN_UNSUPPORTED, "dtype must be fp32 or bf16");
+  if (D != 64 && D != 128) return fail(CPATTN_UNSUPPORTED, "head dim D must be 64 or 128");
+  if (H < 1 || Hkv < 1 || H > 256 || Hkv > 256) return fail(CPATTN_INVALID_ARG, "H and Hkv must be in [1, 256]");
+  if (H % Hkv != 0) return fail(CPATTN_INVALID_ARG, "H must be a multiple of Hkv");
+  return CPATTN_OK;
+}
+
+void tile_sizes(cpattn_dtype_t dt, int* tm, int* tn) {
+  if (dt == CPATTN_DTYPE_BF16) {
+    *tm = cpattn::kTcTileM;
+    *tn = cpattn::kTcTileN;
+  } else {
+    *tm = cpattn::kSimtTileM;
+    *tn = cpattn::kSimtTileN;
+  }
+}
+
+// Host staging of a work list (and the plan's index map) in pinned memory,
+// so the per-call upload is a true asynchronous copy.  Kept per work list;
+// freed with the plan.
+struct Pinned {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+
+struct PlanExtras {
+  std::map<const WorkList*, Pinned> worklists;
+  Pinned index_map;
+};
+
+std::mutex g_extras_mu;
+std::map<const cpattn_plan_t*, PlanExtras> g_extras;
+
+cpattn_status_t pinned_copy(const void* src, size_t bytes, Pinned* out) {
+  if (out->ptr) return CPATTN_OK;
+  if (bytes == 0) return CPATTN_OK;
+  cudaError_t e = cudaMallocHost(&out->ptr, bytes);
+  if (e != cudaSuccess) {
+    out->ptr = nullptr;
+    return cuda_fail(e, "cudaMallocHost (work-list staging)");
+  }
+  memcpy(out->ptr, src, bytes);
+  out->bytes = bytes;
+  return CPATTN_OK;
+}
+
+// Upload the work list (tiles then runs, at their workspace offsets) and clear the fault word.
+cpattn_status_t upload_worklist(const cpattn_plan_t* plan, const WorkList& wl, const WsLayout& L, uint8_t* ws,
+                                cudaStream_t stream) {
+  const size_t tb = wl.tiles.size() * sizeof(QTile), rb = wl.runs.size() * sizeof(KvRun);
+  Pinned pt;
+  {
+    std::lock_guard<std::mutex> lock(g_extras_mu);
+    Pinned& slot = g_extras[plan].worklists[&wl];
+    if (!slot.ptr && tb + rb > 0) {
+      std::vector<uint8_t> buf(L.runs - L.tiles + rb);
+      if (tb) memcpy(buf.data(), wl.tiles.data(), tb);
+      if (rb) memcpy(buf.data() + (L.runs - L.tiles), wl.runs.data(), rb);
+      cpattn_status_t s = pinned_copy(buf.data(), buf.size(), &slot);
+      if (s != CPATTN_OK) return s;
+    }
+    pt = slot;
+  }
+  cudaError_t e = cudaMemsetAsync(ws, 0, CPATTN_WS_HEADER_BYTES, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (fault word)");
+  if (pt.ptr) {
+    e = cudaMemcpyAsync(ws + L.tiles, pt.ptr, pt.bytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (work list)");
+  }
+  return CPATTN_OK;
+}
+
+cpattn_status_t upload_index_map(const cpattn_plan_t* plan, uint8_t* dst, cudaStream_t stream) {
+  Pinned pm;
+  {
+    std::lock_guard<std::mutex> lock(g_extras_mu);
+    Pinned& slot = g_extras[plan].index_map;
+    cpattn_status_t s = pinned_copy(plan->index_map.data(), plan->index_map.size() * sizeof(int64_t), &slot);
+    if (s != CPATTN_OK) return s;
+    pm = slot;
+  }
+  cudaError_t e = cudaMemcpyAsync(dst, pm.ptr, pm.bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (index map)");
+  return CPATTN_OK;
+}
+
+cpattn_status_t launch_attention(cpattn::AttnArgs& a, cpattn_dtype_t dt) {
+  std::string err;
+  cudaError_t e = (dt == CPATTN_DTYPE_BF16) ? cpattn::launch_attn_bf16_tc(a, &err) : cpattn::launch_attn_fp32_simt(a, &err);
+  if (e != cudaSuccess) {
+    if (!err.empty()) return fail(CPATTN_INVALID_ARG, err);
+    return cuda_fail(e, "attention kernel launch");
+  }
+  return CPATTN_OK;
+}
+
+// Common checks and setup for cpattn_fwd / cpattn_block_fwd.
+cpattn_status_t prepare(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
+                        cpattn_dtype_t dtype, int32_t H, int32_t Hkv, int32_t D, int32_t causal, void* ws,
+                        size_t ws_bytes) {
+  if (!plan) return fail(CPATTN_INVALID_ARG, "plan is NULL");
+  cpattn_status_t s = check_shape(H, Hkv, D, dtype);
+  if (s != CPATTN_OK) return s;
+  if (!q || !k || !v) return fail(CPATTN_INVALID_ARG, "q, k and v must be device pointers");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return fail(CPATTN_INVALID_ARG, "q, k, v must be 16-byte aligned");
+  if (causal && plan->mode == CPATTN_MODE_GRID2D)
+    return fail(CPATTN_UNSUPPORTED, "causal masks are not defined for grid2d plans");
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return fail(CPATTN_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
+  (void)ws_bytes;
+  return CPATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cpattn_status_t cpattn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t cp_size, cpattn_mode_t mode,
+                            const cpattn_grid_t* grid, cpattn_plan_t** out_plan) {
+  if (!out_plan) return fail(CPATTN_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  auto* p = new (std::nothrow) cpattn_plan_t();
+  if (!p) return fail(CPATTN_INVALID_ARG, "out of host memory");
+  int32_t g[3] = {0, 0, 0};
+  if (grid) {
+    g[0] = grid->frames;
+    g[1] = grid->height;
+    g[2] = grid->width;
+  }
+  std::string err;
+  try {
+    err = cpattn::build_plan(cu_seqlens_host, n_seqs, cp_size, (int32_t)mode, grid ? g : nullptr, p);
+  } catch (const std::exception& ex) {
+    err = std::string("planner failed: ") + ex.what();
+  }
+  if (!err.empty()) {
+    delete p;
+    return fail(CPATTN_INVALID_ARG, err);
+  }
+  *out_plan = p;
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_plan_destroy(cpattn_plan_t* plan) {
+  if (!plan) return CPATTN_OK;
+  {
+    std::lock_guard<std::mutex> lock(g_extras_mu);
+    auto it = g_extras.find(plan);
+    if (it != g_extras.end()) {
+      // cudaFreeHost waits for copies that still read the staging buffers
+      for (auto& kv : it->second.worklists)
+        if (kv.second.ptr) cudaFreeHost(kv.second.ptr);
+      if (it->second.index_map.ptr) cudaFreeHost(it->second.index_map.ptr);
+      g_extras.erase(it);
+    }
+  }
+  delete plan;
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_plan_get_info(const cpattn_plan_t* plan, cpattn_plan_info_t* out) {
+  if (!plan || !out) return fail(CPATTN_INVALID_ARG, "NULL argument");
+  memset(out, 0, sizeof(*out));
+  out->total_tokens = plan->T;
+  out->n_chunks = (int64_t)plan->chunk_ranks.size();
+  int64_t mx = 0;
+  for (int r = 0; r < plan->cp; ++r) mx = std::max<int64_t>(mx, plan->rank_offsets[r + 1] - plan->rank_offsets[r]);
+  out->max_rank_tokens = mx;
+  out->n_seqs = plan->n_seqs;
+  out->cp_size = plan->cp;
+  out->mode = plan->mode;
+  out->split_h = plan->split_h;
+  out->split_w = plan->split_w;
+  return CPATTN_OK;
+}
+
+#define CPATTN_COPY_OUT(vec)                                                         \
+  do {                                                                               \
+    if (!plan || !out) return fail(CPATTN_INVALID_ARG, "NULL argument");             \
+    if (n < (int64_t)(vec).size()) return fail(CPATTN_INVALID_ARG, "output too small"); \
+    if (!(vec).empty()) memcpy(out, (vec).data(), (vec).size() * sizeof((vec)[0]));  \
+    return CPATTN_OK;                                                                \
+  } while (0)
+
+cpattn_status_t cpattn_plan_get_chunk_offsets(const cpattn_plan_t* plan, int64_t* out, int64_t n) {
+  CPATTN_COPY_OUT(plan->chunk_offsets);
+}
+cpattn_status_t cpattn_plan_get_chunk_ranks(const cpattn_plan_t* plan, int32_t* out, int64_t n) {
+  CPATTN_COPY_OUT(plan->chunk_ranks);
+}
+cpattn_status_t cpattn_plan_get_rank_offsets(const cpattn_plan_t* plan, int64_t* out, int64_t n) {
+  CPATTN_COPY_OUT(plan->rank_offsets);
+}
+cpattn_status_t cpattn_plan_get_index_map(const cpattn_plan_t* plan, int64_t* out, int64_t n) {
+  CPATTN_COPY_OUT(plan->index_map);
+}
+
+cpattn_status_t cpattn_plan_get_local_cu_seqlens(const cpattn_plan_t* plan, int32_t rank, int32_t* out, int64_t n) {
+  if (!plan || !out) return fail(CPATTN_INVALID_ARG, "NULL argument");
+  if (rank < 0 || rank >= plan->cp) return fail(CPATTN_INVALID_ARG, "rank out of range");
+  if (n < plan->n_seqs + 1) return fail(CPATTN_INVALID_ARG, "output too small");
+  memcpy(out, &plan->local_cu[(size_t)rank * (plan->n_seqs + 1)], sizeof(int32_t) * (plan->n_seqs + 1));
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_plan_get_ring_schedule(const cpattn_plan_t* plan, int32_t causal, int32_t* kv_rank,
+                                              int32_t* mask_kind, int64_t n) {
+  if (!plan || !kv_rank || !mask_kind) return fail(CPATTN_INVALID_ARG, "NULL argument");
+  const int cp = plan->cp;
+  if (n < (int64_t)cp * cp) return fail(CPATTN_INVALID_ARG, "output too small");
+  for (int r = 0; r < cp; ++r)
+    for (int t = 0; t < cp; ++t)
+      if (!cpattn::ring_entry(*plan, r, t, causal != 0, &kv_rank[r * cp + t], &mask_kind[r * cp + t]))
+        return fail(CPATTN_UNSUPPORTED, "causal masks are not defined for grid2d plans");
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_workspace_size(const cpattn_plan_t* plan, int32_t H, int32_t Hkv, int32_t D,
+                                      cpattn_dtype_t dtype, int32_t causal, size_t* bytes) {
+  if (!plan || !bytes) return fail(CPATTN_INVALID_ARG, "NULL argument");
+  cpattn_status_t s = check_shape(H, Hkv, D, dtype);
+  if (s != CPATTN_OK) return s;
+  if (causal && plan->mode == CPATTN_MODE_GRID2D)
+    return fail(CPATTN_UNSUPPORTED, "causal masks are not defined for grid2d plans");
+  int tm, tn;
+  tile_sizes(dtype, &tm, &tn);
+  auto wl = cpattn::get_worklist(*const_cast<cpattn_plan_t*>(plan), causal != 0, tm, tn, -1, 0);
+  *bytes = ws_layout(*plan, *wl, H, Hkv, D, elem_size(dtype)).total;
+  return CPATTN_OK;
+}
+
+static cpattn_status_t run_attention(const cpattn_plan_t* cplan, const void* q, const void* k, const void* v,
+                                     cpattn_dtype_t dtype, int32_t H, int32_t Hkv, int32_t D, float scale,
+                                     int32_t causal, int q_rank, int step, void* o, float* lse, void* workspace,
+                                     size_t ws_bytes, void* stream_ptr) {
+  cpattn_status_t s = prepare(cplan, q, k, v, dtype, H, Hkv, D, causal, workspace, ws_bytes);
+  if (s != CPATTN_OK) return s;
+  if (!o || !lse) return fail(CPATTN_INVALID_ARG, "o and lse must be device pointers");
+  if (!aligned16(o)) return fail(CPATTN_INVALID_ARG, "o must be 16-byte aligned");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CPATTN_INVALID_ARG, "scale must be positive and finite");
+  cpattn_plan_t* plan = const_cast<cpattn_plan_t*>(cplan);
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int tm, tn;
+  tile_sizes(dtype, &tm, &tn);
+  // the workspace must hold the whole-forward layout (an upper bound for one step)
+  auto wl_all = cpattn::get_worklist(*plan, causal != 0, tm, tn, -1, 0);
+  const size_t es = elem_size(dtype);
+  const WsLayout L_all = ws_layout(*plan, *wl_all, H, Hkv, D, es);
+  if (ws_bytes < L_all.total)
+    return fail(CPATTN_WORKSPACE, "workspace too small: need " + std::to_string(L_all.total) + " bytes");
+  auto wl = (q_rank < 0) ? wl_all : cpattn::get_worklist(*plan, causal != 0, tm, tn, q_rank, step);
+  WsLayout L = ws_layout(*plan, *wl, H, Hkv, D, es);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  s = upload_worklist(plan, *wl, L, ws, stream);
+  if (s != CPATTN_OK) return s;
+
+  cpattn::AttnArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.q_rows_total = plan->T;
+  a.kv_rows_total = plan->T;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.scale = scale;
+  a.tiles = reinterpret_cast<const QTile*>(ws + L.tiles);
+  a.runs = reinterpret_cast<const KvRun*>(ws + L.runs);
+  a.n_tiles = (int32_t)wl->tiles.size();
+  a.o = o;
+  a.lse = lse;
+  a.ws = reinterpret_cast<WsHeader*>(ws);
+  a.stream = stream;
+  if (q_rank < 0) {
+    a.partial = false;
+    a.lse_ld = plan->T;
+  } else {
+    a.partial = true;
+    a.lse_ld = plan->rank_offsets[q_rank + 1] - plan->rank_offsets[q_rank];
+  }
+  if (plan->mode == CPATTN_MODE_GRID2D) {
+    // split_cp_2d: gather every rank's shard into contiguous rows
+    uint8_t* idx = ws + L_all.idx;
+    s = upload_index_map(plan, idx, stream);
+    if (s != CPATTN_OK) return s;
+    const int64_t* index = reinterpret_cast<const int64_t*>(idx);
+    cudaError_t e;
+    e = cpattn::launch_permute_rows(q, ws + L_all.q, index, plan->T, (int64_t)H * D * es, plan->T, false, stream);
+    if (e == cudaSuccess)
+      e = cpattn::launch_permute_rows(k, ws + L_all.k, index, plan->T, (int64_t)Hkv * D * es, plan->T, false, stream);
+    if (e == cudaSuccess)
+      e = cpattn::launch_permute_rows(v, ws + L_all.v, index, plan->T, (int64_t)Hkv * D * es, plan->T, false, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "shard gather");
+    a.q = ws + L_all.q;
+    a.k = ws + L_all.k;
+    a.v = ws + L_all.v;
+    // gather_cp_2d: the final outputs go back to global rows through the index map
+    if (q_rank < 0) a.out_map = index;
+  }
+  return launch_attention(a, dtype);
+}
+
+cpattn_status_t cpattn_fwd(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
+                           cpattn_dtype_t dtype, int32_t H, int32_t Hkv, int32_t D, float scale, int32_t causal,
+                           void* o, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  return run_attention(plan, q, k, v, dtype, H, Hkv, D, scale, causal, -1, 0, o, lse, workspace, ws_bytes, stream);
+}
+
+cpattn_status_t cpattn_block_fwd(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
+                                 cpattn_dtype_t dtype, int32_t H, int32_t Hkv, int32_t D, float scale, int32_t causal,
+                                 int32_t q_rank, int32_t ring_step, float* o_partial, float* lse_partial,
+                                 void* workspace, size_t ws_bytes, void* stream) {
+  if (!plan) return fail(CPATTN_INVALID_ARG, "plan is NULL");
+  if (q_rank < 0 || q_rank >= plan->cp) return fail(CPATTN_INVALID_ARG, "q_rank out of range");
+  if (ring_step < 0 || ring_step >= plan->cp) return fail(CPATTN_INVALID_ARG, "ring_step out of range");
+  return run_attention(plan, q, k, v, dtype, H, Hkv, D, scale, causal, q_rank, ring_step, o_partial, lse_partial,
+                       workspace, ws_bytes, stream);
+}
+
+cpattn_status_t cpattn_merge(int32_t n_partials, const float* const* o_parts_host, const float* const* lse_parts_host,
+                             int64_t rows, int32_t H, int32_t D, const int64_t* out_rows, int64_t out_total_rows,
+                             void* o_out, cpattn_dtype_t out_dtype, float* lse_out, void* stream) {
+  if (n_partials < 1 || n_partials > 64) return fail(CPATTN_INVALID_ARG, "n_partials must be in [1, 64]");
+  if (!o_parts_host || !lse_parts_host || !o_out || !lse_out) return fail(CPATTN_INVALID_ARG, "NULL argument");
+  if (D != 64 && D != 128) return fail(CPATTN_UNSUPPORTED, "head dim D must be 64 or 128");
+  if (H < 1 || rows < 0) return fail(CPATTN_INVALID_ARG, "bad rows or H");
+  if (out_dtype != CPATTN_DTYPE_FP32 && out_dtype != CPATTN_DTYPE_BF16) return fail(CPATTN_UNSUPPORTED, "out dtype");
+  if (!out_rows && out_total_rows < rows) return fail(CPATTN_INVALID_ARG, "out_total_rows < rows");
+  if (!aligned16(o_out)) return fail(CPATTN_INVALID_ARG, "o_out must be 16-byte aligned");
+  cpattn::MergeArgs a;
+  a.n = n_partials;
+  for (int i = 0; i < n_partials; ++i) {
+    if (!o_parts_host[i] || !lse_parts_host[i] || !aligned16(o_parts_host[i]))
+      return fail(CPATTN_INVALID_ARG, "partial pointers must be non-NULL, O partials 16-byte aligned");
+    a.o_parts[i] = o_parts_host[i];
+    a.lse_parts[i] = lse_parts_host[i];
+  }
+  a.rows = rows;
+  a.H = H;
+  a.D = D;
+  a.out_rows = out_rows;
+  a.out_total_rows = out_total_rows;
+  a.o_out = o_out;
+  a.out_bf16 = out_dtype == CPATTN_DTYPE_BF16;
+  a.lse_out = lse_out;
+  a.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cpattn::launch_merge(a);
+  if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+  return CPATTN_OK;
+}
+
+static cpattn_status_t permute(const void* src, void* dst, const int64_t* index, int64_t rows, int64_t row_bytes,
+                               int64_t other_rows, bool scatter, void* stream) {
+  if (!src || !dst || (!index && rows > 0)) return fail(CPATTN_INVALID_ARG, "NULL argument");
+  if (rows < 0 || other_rows < 0) return fail(CPATTN_INVALID_ARG, "negative row count");
+  if (row_bytes <= 0 || (row_bytes & 15)) return fail(CPATTN_INVALID_ARG, "row_bytes must be a positive multiple of 16");
+  if (!aligned16(src) || !aligned16(dst)) return fail(CPATTN_INVALID_ARG, "src and dst must be 16-byte aligned");
+  cudaError_t e = cpattn::launch_permute_rows(src, dst, index, rows, row_bytes, other_rows, scatter,
+                                              static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "permute kernel launch");
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_gather_rows(const void* src, int64_t src_rows, void* dst, const int64_t* index, int64_t rows,
+                                   int64_t row_bytes, void* stream) {
+  return permute(src, dst, index, rows, row_bytes, src_rows, false, stream);
+}
+
+cpattn_status_t cpattn_scatter_rows(const void* src, void* dst, int64_t dst_rows, const int64_t* index, int64_t rows,
+                                    int64_t row_bytes, void* stream) {
+  return permute(src, dst, index, rows, row_bytes, dst_rows, true, stream);
+}
+
+cpattn_status_t cpattn_token_loss_norm(const float* loss, const uint8_t* valid, int64_t T, double* out_loss,
+                                       int64_t* out_count, float* out_loss_f32, void* stream) {
+  if (T < 0) return fail(CPATTN_INVALID_ARG, "T must be >= 0");
+  if ((T > 0 && (!loss || !valid)) || !out_loss || !out_count) return fail(CPATTN_INVALID_ARG, "NULL argument");
+  cudaError_t e = cpattn::launch_loss_norm(loss, valid, T, out_loss, out_count, out_loss_f32,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "loss kernel launch");
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_fwd_flops(const int32_t* cu, int32_t n_seqs, int32_t H, int32_t D, int32_t causal,
+                                 uint64_t* out_u64, double* out_f64) {
+  if (!cu || n_seqs < 1 || H < 1 || D < 1) return fail(CPATTN_INVALID_ARG, "bad arguments");
+  unsigned __int128 pairs = 0;
+  for (int s = 0; s < n_seqs; ++s) {
+    const int64_t L = (int64_t)cu[s + 1] - cu[s];
+    if (L < 0) return fail(CPATTN_INVALID_ARG, "cu_seqlens must be non-decreasing");
+    pairs += causal ? (unsigned __int128)L * (L + 1) / 2 : (unsigned __int128)L * L;
+  }
+  const unsigned __int128 f = pairs * 4u * (unsigned)D * (unsigned)H;
+  if (f > (unsigned __int128)UINT64_MAX) return fail(CPATTN_INVALID_ARG, "FLOP count overflows uint64");
+  if (out_u64) *out_u64 = (uint64_t)f;
+  if (out_f64) *out_f64 = (double)(uint64_t)f;
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_sync_status(const void* workspace, void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  if (workspace) {
+    WsHeader h;
+    e = cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the fault word");
+    if (h.fault != 0)
+      return fail(CPATTN_DEVICE_FAULT, "kernel fault " + std::to_string(h.fault) + " in block " +
+                                           std::to_string(h.info) + " at " + std::to_string(h.detail));
+  }
+  return CPATTN_OK;
+}
+
+const char* cpattn_last_error_string(void) { return g_err.c_str(); }
+
+const char* cpattn_version(void) { return "cpattn 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,472 @@
+// bf16 packed varlen attention forward on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in TMEM, K/V/Q tiles staged by TMA).
+//
+// One thread block computes one 128-row query tile of one head.  It walks the
+// tile's KV runs in ring order - at ring step t the queries of virtual rank r
+// see the KV shard of rank (r - t) mod cp ("Scaling video training with
+// parallelism", section 2, Ring Attention) - in 128-key tiles, and merges
+// every tile's partial into the running result by exact log-sum-exp
+// rescaling, so each ring step's partial (O_t, lse_t) is folded in as soon as
+// it is produced and never leaves the SM.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q once, then K and V tiles through NS-deep rings
+//               (K one tile ahead of V, matching the order they are consumed).
+//   warp 1      TMEM allocator and MMA issuer (one thread):
+//                 S_j = Q K_j^T   (M=128, N=128, K=D)   into TMEM S[j%2]
+//                 O  += P_j V_j   (M=128, N=D,   K=128) into TMEM O
+//               S_{j+1} is issued before PV_j so the tensor core computes the
+//               next scores while the softmax warps work on this tile.
+//   warps 2-5   softmax + epilogue, one query row per thread: read S from
+//               TMEM, apply the causal / run-end mask from token positions,
+//               update the running max and sum, write P (bf16) to shared
+//               memory in the 128-byte-swizzled K-major layout the MMA reads,
+//               and rescale O in TMEM when the running max moves by more than
+//               2^8 (otherwise the stale max is kept: O and the sum share it,
+//               so the final O/l is exact).
+//
+// Shared-memory operand layouts (all 1024-byte aligned, SWIZZLE_128B):
+//   Q, K: [128 rows][64 columns] boxes, K-major (rows = M or N, columns = K).
+//   V:    [128 keys][64 d] boxes; as the B operand of P.V (N = d, K = keys)
+//         this is MN-major: 8-key groups 1024 B apart (SBO), 64-wide d
+//         blocks one box apart (LBO).
+//   P:    [128 rows][64 keys] x 2 boxes, K-major, written by the softmax warps.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.hpp"
+
+namespace cpattn {
+
+using namespace dev;
+
+struct alignas(64) TcParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  const QTile* tiles;
+  const KvRun* runs;
+  void* o;
+  float* lse;
+  const int64_t* out_map;
+  WsHeader* ws;
+  int64_t lse_ld;
+  int32_t H, Hkv;
+  float scale;        // softmax scale (natural-log domain)
+  float scale_log2;   // scale * log2(e)
+  float thresh_raw;   // 8 / scale_log2: raw-score growth that forces a rescale
+};
+
+template <int D>
+struct TcCfg {
+  static constexpr int KB = D / 64;                 // 64-column boxes per row
+  static constexpr int NS = (D == 128) ? 2 : 4;     // K and V ring depth
+  static constexpr uint32_t BOX = 128 * 128;        // 128 rows x 128 bytes
+  static constexpr uint32_t Q_BYTES = KB * BOX;
+  static constexpr uint32_t KV_BYTES = KB * BOX;
+  static constexpr uint32_t OFF_K = Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + NS * KV_BYTES;
+  static constexpr uint32_t OFF_P = OFF_V + NS * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_P + 2 * BOX;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;
+  static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;              // S0 | S1 | O
+  static constexpr uint32_t TM_S = 0, TM_O = 256;
+};
+
+// Advances through the KV runs of a q tile in 128-key steps.
+struct KvCursor {
+  int r, off;
+  __device__ void next(const KvRun* runs) {
+    off += 128;
+    if (off >= runs[r].kv_len) {
+      ++r;
+      off = 0;
+    }
+  }
+};
+
+template <int D, bool kPartial>
+__global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
+  using C = TcCfg<D>;
+  constexpr int NS = C::NS;
+  constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = q_full + 1;
+  uint64_t* k_empty = k_full + NS;
+  uint64_t* v_full = k_empty + NS;
+  uint64_t* v_empty = v_full + NS;
+  uint64_t* s_full = v_empty + NS;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* o_done = p_full + 1;
+  uint64_t* drain = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+  int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);  // [0] K loads, [1] V loads, [2] Q
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_id = blockIdx.x / p.H;
+  const int h = blockIdx.x - tile_id * p.H;
+  const int g = h / (p.H / p.Hkv);
+  const QTile tile = p.tiles[tile_id];
+  const int n_kv = tile.n_kv_tiles;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(k_full + i, 1);
+      mbar_init(k_empty + i, 1);
+      mbar_init(v_full + i, 1);
+      mbar_init(v_empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(s_free + i, 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    issued[0] = issued[1] = issued[2] = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_kv > 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      for (int kb = 0; kb < C::KB; ++kb)
+        tma_load_3d(smem + kb * C::BOX, &p.tm_q, q_full, kb * 64, h, tile.q_row0);
+      issued[2] = 1;
+      KvCursor ck{tile.run_begin, 0}, cv{tile.run_begin, 0};
+      int jk = 0, jv = 0;
+      while (jk < n_kv || jv < n_kv) {
+        if (jk < n_kv && jk <= jv + 1) {
+          const int st = jk % NS;
+          if (jk >= NS && !wait_bounded(k_empty + st, ((jk / NS) - 1) & 1, abort_flag, p.ws, 1)) break;
+          const int row = p.runs[ck.r].kv_row0 + ck.off;
+          mbar_arrive_expect_tx(k_full + st, C::KV_BYTES);
+          uint8_t* dst = smem + C::OFF_K + st * C::KV_BYTES;
+          for (int kb = 0; kb < C::KB; ++kb) tma_load_3d(dst + kb * C::BOX, &p.tm_k, k_full + st, kb * 64, g, row);
+          ck.next(p.runs);
+          issued[0] = ++jk;
+        } else {
+          const int st = jv % NS;
+          if (jv >= NS && !wait_bounded(v_empty + st, ((jv / NS) - 1) & 1, abort_flag, p.ws, 2)) break;
+          const int row = p.runs[cv.r].kv_row0 + cv.off;
+          mbar_arrive_expect_tx(v_full + st, C::KV_BYTES);
+          uint8_t* dst = smem + C::OFF_V + st * C::KV_BYTES;
+          for (int kb = 0; kb < C::KB; ++kb) tma_load_3d(dst + kb * C::BOX, &p.tm_v, v_full + st, kb * 64, g, row);
+          cv.next(p.runs);
+          issued[1] = ++jv;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_kv > 0) {
+      const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + C::OFF_K);
+      const uint32_t sV = smem_u32(smem + C::OFF_V), sP = smem_u32(smem + C::OFF_P);
+      auto issue_s = [&](int i) {
+        const uint32_t d = tmem + C::TM_S + 128u * (i & 1);
+        const uint32_t kbase = sK + (i % NS) * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::BOX + (kk & 3) * 32;
+          umma_bf16_ss(d, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024), IDESC_S,
+                       kk > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = wait_bounded(q_full, 0, abort_flag, p.ws, 3) && wait_bounded(k_full, 0, abort_flag, p.ws, 4);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        if (NS < n_kv) umma_commit(k_empty);
+        umma_commit(s_full);
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (j + 1 < n_kv) {
+          const int i = j + 1, st = i % NS;
+          ok = wait_bounded(k_full + st, (i / NS) & 1, abort_flag, p.ws, 5);
+          if (ok && i >= 2) ok = wait_bounded(s_free + (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.ws, 6);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(i);
+          if (i + NS < n_kv) umma_commit(k_empty + st);
+          umma_commit(s_full + (i & 1));
+        }
+        ok = wait_bounded(p_full, j & 1, abort_flag, p.ws, 7) &&
+             wait_bounded(v_full + (j % NS), (j / NS) & 1, abort_flag, p.ws, 8);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vbase = sV + (j % NS) * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t aoff = (kk >> 2) * C::BOX + (kk & 3) * 32;  // P: 16 keys inside a 64-key box
+          const uint32_t boff = kk * 2048;                          // V: 16 keys = two 8-row groups
+          umma_bf16_ss(tmem + C::TM_O, smem_desc_sw128(sP + aoff, 16, 1024),
+                       smem_desc_sw128(vbase + boff, C::BOX, 1024), IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (j + NS < n_kv) umma_commit(v_empty + (j % NS));
+        umma_commit(o_done);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t sP = smem_u32(smem + C::OFF_P);
+    const int q_pos = tile.q_pos0 + row;
+    const float c2 = p.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    KvCursor cur{tile.run_begin, 0};
+    for (int j = 0; j < n_kv; ++j) {
+      const KvRun run = p.runs[cur.r];
+      const int n_keys = min(128, run.kv_len - cur.off);
+      const int kpos0 = run.kv_pos0 + cur.off;
+      const bool tile_mask = (n_keys < 128) || (run.causal && kpos0 + n_keys - 1 > tile.q_pos0);
+      cur.next(p.runs);
+
+      if (!__all_sync(0xffffffffu, wait_bounded(s_full + (j & 1), (j >> 1) & 1, abort_flag, p.ws, 9))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld128_wait(tl + C::TM_S + 128u * (j & 1), sr);
+      tc_fence_before();
+      mbar_arrive(s_free + (j & 1));
+
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+      if (tile_mask) {
+        int lim = n_keys;
+        if (run.causal) lim = min(lim, q_pos - kpos0 + 1);
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+
+      float alpha = 1.f;
+      bool scale_o = false;
+      if (mx > m_ref + p.thresh_raw) {
+        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx((m_ref - mx) * c2);
+        scale_o = (j > 0) && (m_ref != -INFINITY);
+        m_ref = mx;
+        l *= alpha;
+      }
+      const float mc = (m_ref == -INFINITY) ? 0.f : m_ref * c2;
+      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 4) {
+        s[c] = ex2_approx(fmaf(s[c], c2, -mc));
+        s[c + 1] = ex2_approx(fmaf(s[c + 1], c2, -mc));
+        s[c + 2] = ex2_approx(fmaf(s[c + 2], c2, -mc));
+        s[c + 3] = ex2_approx(fmaf(s[c + 3], c2, -mc));
+        rs0 += s[c];
+        rs1 += s[c + 1];
+        rs2 += s[c + 2];
+        rs3 += s[c + 3];
+      }
+      l += (rs0 + rs1) + (rs2 + rs3);
+
+      // P and O may only change once PV_{j-1} has finished reading/writing them.
+      if (j > 0) {
+        if (!__all_sync(0xffffffffu, wait_bounded(o_done, (j - 1) & 1, abort_flag, p.ws, 10))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int cc = 0; cc < 16; ++cc) {
+        const uint32_t addr = sP + (cc >> 3) * C::BOX + row * 128 + ((((uint32_t)cc & 7u) ^ ((uint32_t)row & 7u)) << 4);
+        st_shared_v4(addr, pack_bf16x2(s[8 * cc + 0], s[8 * cc + 1]), pack_bf16x2(s[8 * cc + 2], s[8 * cc + 3]),
+                     pack_bf16x2(s[8 * cc + 4], s[8 * cc + 5]), pack_bf16x2(s[8 * cc + 6], s[8 * cc + 7]));
+      }
+      if (__any_sync(0xffffffffu, scale_o)) {
+        const float a = scale_o ? alpha : 1.f;
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t o[32];
+          tmem_ld32_wait(tl + C::TM_O + 32u * cb, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+          tmem_st32(tl + C::TM_O + 32u * cb, o);
+        }
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+
+    if (ok && n_kv > 0) {
+      ok = __all_sync(0xffffffffu, wait_bounded(o_done, (n_kv - 1) & 1, abort_flag, p.ws, 11));
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      const bool valid_row = row < tile.q_rows;
+      const bool has = l > 0.f;
+      const float inv_l = has ? 1.f / l : 0.f;
+      const int64_t out_row = p.out_map ? p.out_map[tile.out_row0 + (valid_row ? row : 0)]
+                                        : (int64_t)tile.out_row0 + row;
+#pragma unroll
+      for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t o[32];
+        if (n_kv > 0) {
+          tmem_ld32_wait(tl + C::TM_O + 32u * cb, o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        if (valid_row) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = has ? __uint_as_float(o[i]) * inv_l : 0.f;
+          if (kPartial) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + (out_row * p.H + h) * D + 32 * cb);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (out_row * p.H + h) * D + 32 * cb);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+          }
+        }
+      }
+      if (valid_row) p.lse[(int64_t)h * p.lse_ld + out_row] = has ? m_ref * p.scale + logf(l) : -INFINITY;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // Let copies and MMAs already in flight land before the block exits.
+    if (warp == 0 && lane == 0) {
+      if (issued[2]) drain_wait(q_full, 0);
+      for (int j = max(0, issued[0] - NS); j < issued[0]; ++j) drain_wait(k_full + (j % NS), (j / NS) & 1);
+      for (int j = max(0, issued[1] - NS); j < issued[1]; ++j) drain_wait(v_full + (j % NS), (j / NS) & 1);
+    }
+    if (warp == 1 && lane == 0 && n_kv > 0) {
+      umma_commit(drain);
+      drain_wait(drain, 0);
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [rows, heads, D] bf16 viewed as a 3-D tensor (D, heads, rows); box = 64
+// columns x 1 head x 128 rows, 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, std::string* err) {
+  auto enc = tensor_map_encoder();
+  if (!enc) {
+    *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
+    return false;
+  }
+  return true;
+}
+
+template <int D, bool kPartial>
+static cudaError_t launch_tc(const TcParams& p, int n_blocks, cudaStream_t stream) {
+  auto kern = attn_fwd_tc_kernel<D, kPartial>;
+  const uint32_t smem = TcCfg<D>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<n_blocks, 192, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bf16_tc(const AttnArgs& a, std::string* err) {
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_map(&p.tm_q, a.q, a.q_rows_total, a.H, a.D, err) ||
+      !make_map(&p.tm_k, a.k, a.kv_rows_total, a.Hkv, a.D, err) ||
+      !make_map(&p.tm_v, a.v, a.kv_rows_total, a.Hkv, a.D, err))
+    return cudaErrorInvalidValue;
+  p.tiles = a.tiles;
+  p.runs = a.runs;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.out_map = a.out_map;
+  p.ws = a.ws;
+  p.lse_ld = a.lse_ld;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.thresh_raw = 8.0f / p.scale_log2;
+  const int64_t blocks = (int64_t)a.n_tiles * a.H;
+  if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7fffffff) {
+    *err = "too many query tiles";
+    return cudaErrorInvalidValue;
+  }
+  if (a.D == 128) return a.partial ? launch_tc<128, true>(p, (int)blocks, a.stream)
+                                   : launch_tc<128, false>(p, (int)blocks, a.stream);
+  return a.partial ? launch_tc<64, true>(p, (int)blocks, a.stream) : launch_tc<64, false>(p, (int)blocks, a.stream);
+}
+
+}  // namespace cpattn

@@ -1,0 +1,67 @@
+// Launch descriptors for the CUDA kernels (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "worklist.h"
+
+namespace cpattn {
+
+// One attention launch over a work list.  Q/K/V are [rows, heads, D]
+// buffers (global THD tensors, or gathered shards for GRID2D).
+struct AttnArgs {
+  const void* q = nullptr;
+  const void* k = nullptr;
+  const void* v = nullptr;
+  int64_t q_rows_total = 0;   // rows in the Q buffer
+  int64_t kv_rows_total = 0;  // rows in the K/V buffers
+  int32_t H = 0, Hkv = 0, D = 0;
+  float scale = 0.f;
+  const QTile* tiles = nullptr;  // device
+  const KvRun* runs = nullptr;   // device
+  int32_t n_tiles = 0;
+  void* o = nullptr;             // final: dtype [*,H,D] at global rows; partial: fp32 [*,H,D]
+  bool partial = false;
+  float* lse = nullptr;          // [H, lse_ld]
+  int64_t lse_ld = 0;
+  const int64_t* out_map = nullptr;  // optional: output row = out_map[row]
+  WsHeader* ws = nullptr;
+  cudaStream_t stream = nullptr;
+};
+
+// q tile / kv tile sizes each attention kernel was built for
+constexpr int kTcTileM = 128, kTcTileN = 128;
+constexpr int kSimtTileM = 64, kSimtTileN = 32;
+
+cudaError_t launch_attn_bf16_tc(const AttnArgs& a, std::string* err);
+cudaError_t launch_attn_fp32_simt(const AttnArgs& a, std::string* err);
+
+struct MergeArgs {
+  int32_t n = 0;
+  const float* o_parts[64] = {};
+  const float* lse_parts[64] = {};
+  int64_t rows = 0;
+  int32_t H = 0, D = 0;
+  const int64_t* out_rows = nullptr;
+  int64_t out_total_rows = 0;
+  void* o_out = nullptr;
+  bool out_bf16 = false;
+  float* lse_out = nullptr;
+  cudaStream_t stream = nullptr;
+};
+cudaError_t launch_merge(const MergeArgs& a);
+
+cudaError_t launch_loss_norm(const float* loss, const uint8_t* valid, int64_t T, double* out_loss,
+                             int64_t* out_count, float* out_loss_f32, cudaStream_t stream);
+
+// gather: dst[i] = src[index[i]]; scatter: dst[index[i]] = src[i].  Rows whose
+// index falls outside [0, other_rows) are skipped.
+cudaError_t launch_permute_rows(const void* src, void* dst, const int64_t* index, int64_t rows,
+                                int64_t row_bytes, int64_t other_rows, bool scatter, cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace cpattn

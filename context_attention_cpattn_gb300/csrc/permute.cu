@@ -1,0 +1,46 @@
+// Row permutation between global THD order and per-rank shards: the one-GPU
+// equivalents of LongCat-Video's split_cp_2d (scatter pieces to ranks) and
+// gather_cp_2d (reassemble them) (LongCat-Video context-parallel article,
+// communication primitives).  HBM-bound copy: one warp per row, 16-byte
+// vector loads and stores, grid a multiple of the SM count striding over rows.
+#include "common.cuh"
+#include "kernels.hpp"
+
+namespace cpattn {
+
+namespace {
+
+template <bool kScatter>
+__global__ void __launch_bounds__(256) permute_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                           const int64_t* __restrict__ index, int64_t rows,
+                                                           int64_t row_vecs, int64_t other_rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < rows; i += warps) {
+    const int64_t j = index[i];
+    if (j < 0 || j >= other_rows) continue;  // out-of-range rows are skipped
+    const uint4* s = src + (kScatter ? i : j) * row_vecs;
+    uint4* d = dst + (kScatter ? j : i) * row_vecs;
+    for (int64_t c = lane; c < row_vecs; c += 32) d[c] = s[c];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute_rows(const void* src, void* dst, const int64_t* index, int64_t rows, int64_t row_bytes,
+                                int64_t other_rows, bool scatter, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const int64_t want = (rows + 7) / 8;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  const unsigned blocks = (unsigned)(want < cap ? want : cap);
+  const int64_t vecs = row_bytes / 16;
+  if (scatter)
+    permute_rows_kernel<true><<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                                          index, rows, vecs, other_rows);
+  else
+    permute_rows_kernel<false><<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                                           index, rows, vecs, other_rows);
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

@@ -1,0 +1,269 @@
+// Context-parallel planner (host, integer-only).
+//
+// ZIGZAG: the load-balanced ring split named ZIGZAG-RINGATTN (LongVILA news
+//   article, Fig. 5 and Table 2): each sequence is cut into 2*cp chunks and
+//   rank r keeps chunks r and 2cp-1-r, so that under a causal mask every rank
+//   holds one cheap early chunk and one expensive late chunk.
+// GRID2D: LongCat-Video's 2-D split of a latent by height pieces, then width
+//   pieces, with the closest-to-square factorisation of cp (tensor split
+//   strategy, get_optimal_split).
+// CONTIGUOUS: even contiguous token ranges (token stage of LongVILA MM-SP,
+//   "Scaling video training with parallelism", section 3, Fig. 2).
+#include "plan.hpp"
+
+#include <algorithm>
+#include <cstdio>
+#include <numeric>
+
+#include "../../include/cpattn.h"
+
+namespace cpattn {
+
+void optimal_split(int32_t cp, int32_t* a, int32_t* b) {
+  int32_t s = 1;
+  while ((int64_t)(s + 1) * (s + 1) <= cp) ++s;
+  while (s > 1 && cp % s != 0) --s;
+  *a = s;
+  *b = cp / s;
+}
+
+// Pieces of ceil(n/parts) with the remainder last (torch split(size) rule).
+static bool split_pieces(int64_t n, int32_t parts, std::vector<int64_t>* out) {
+  out->clear();
+  const int64_t size = (n + parts - 1) / parts;
+  for (int64_t left = n; left > 0; left -= size) out->push_back(std::min(size, left));
+  return (int64_t)out->size() == parts;
+}
+
+static void finish_common(cpattn_plan_t* p) {
+  // rank offsets and local cu_seqlens from the per-rank segments
+  const int cp = p->cp, n = p->n_seqs;
+  p->rank_offsets.assign(cp + 1, 0);
+  p->local_cu.assign((size_t)cp * (n + 1), 0);
+  p->index_map.clear();
+  p->index_map.reserve(p->T);
+  for (int r = 0; r < cp; ++r) {
+    int64_t count = 0;
+    std::vector<int64_t> per_seq(n, 0);
+    for (const Segment& s : p->rank_segments[r]) {
+      for (int64_t i = 0; i < s.len; ++i) p->index_map.push_back(s.row0 + i);
+      per_seq[s.seq] += s.len;
+      count += s.len;
+    }
+    p->rank_offsets[r + 1] = p->rank_offsets[r] + count;
+    int32_t* lc = &p->local_cu[(size_t)r * (n + 1)];
+    for (int s = 0; s < n; ++s) lc[s + 1] = lc[s] + (int32_t)per_seq[s];
+  }
+}
+
+std::string build_plan(const int32_t* cu, int32_t n_seqs, int32_t cp, int32_t mode,
+                       const int32_t* grid, cpattn_plan_t* p) {
+  if (!cu) return "cu_seqlens is NULL";
+  if (n_seqs < 1) return "n_seqs must be >= 1";
+  if (cp < 1 || cp > 4096) return "cp_size must be in [1, 4096]";
+  if (cu[0] != 0) return "cu_seqlens[0] must be 0";
+  for (int s = 0; s < n_seqs; ++s)
+    if (cu[s + 1] <= cu[s]) return "cu_seqlens must be strictly increasing";
+  p->mode = mode;
+  p->cp = cp;
+  p->n_seqs = n_seqs;
+  p->T = cu[n_seqs];
+  p->cu.assign(cu, cu + n_seqs + 1);
+  p->rank_segments.assign(cp, {});
+  p->chunk_offsets.clear();
+  p->chunk_ranks.clear();
+  p->split_h = p->split_w = 0;
+
+  if (mode == CPATTN_MODE_ZIGZAG) {
+    const int C = 2 * cp;
+    for (int s = 0; s < n_seqs; ++s) {
+      const int64_t L = (int64_t)cu[s + 1] - cu[s];
+      if (L < C) return "zigzag needs every sequence to have at least 2*cp tokens";
+      const int64_t base = L / C, rem = L % C;
+      std::vector<int64_t> start(C + 1);
+      start[0] = cu[s];
+      for (int j = 0; j < C; ++j) start[j + 1] = start[j] + base + (j < rem ? 1 : 0);
+      for (int j = 0; j < C; ++j) {
+        p->chunk_offsets.push_back(start[j]);
+        p->chunk_ranks.push_back(j < cp ? j : C - 1 - j);
+      }
+      for (int r = 0; r < cp; ++r) {
+        const int lo = r, hi = C - 1 - r;
+        p->rank_segments[r].push_back({start[lo], start[lo + 1] - start[lo], s, start[lo] - cu[s]});
+        p->rank_segments[r].push_back({start[hi], start[hi + 1] - start[hi], s, start[hi] - cu[s]});
+      }
+    }
+    p->chunk_offsets.push_back(p->T);
+  } else if (mode == CPATTN_MODE_GRID2D) {
+    if (!grid) return "grid2d needs a grid";
+    if (n_seqs != 1) return "grid2d plans one latent (n_seqs must be 1)";
+    const int64_t F = grid[0], h = grid[1], w = grid[2];
+    if (F < 1 || h < 1 || w < 1 || F * h * w != p->T) return "grid frames*height*width must equal T";
+    int32_t a, b;
+    optimal_split(cp, &a, &b);
+    const int32_t sh = (h > w) ? b : a, sw = (h > w) ? a : b;
+    std::vector<int64_t> hp, wp;
+    if (!split_pieces(h, sh, &hp)) return "height cannot be cut into split_h pieces";
+    if (!split_pieces(w, sw, &wp)) return "width cannot be cut into split_w pieces";
+    p->split_h = sh;
+    p->split_w = sw;
+    std::vector<int64_t> h0(sh + 1, 0), w0(sw + 1, 0);
+    for (int i = 0; i < sh; ++i) h0[i + 1] = h0[i] + hp[i];
+    for (int i = 0; i < sw; ++i) w0[i + 1] = w0[i] + wp[i];
+    // rank tiles, (f, y, x) row-major inside each tile
+    for (int ih = 0; ih < sh; ++ih)
+      for (int iw = 0; iw < sw; ++iw) {
+        auto& segs = p->rank_segments[ih * sw + iw];
+        for (int64_t f = 0; f < F; ++f)
+          for (int64_t y = h0[ih]; y < h0[ih + 1]; ++y) {
+            const int64_t row = f * h * w + y * w + w0[iw];
+            segs.push_back({row, wp[iw], 0, row});
+          }
+      }
+    // chunks: (frame, row, w-piece) runs in global order
+    for (int64_t f = 0; f < F; ++f)
+      for (int64_t y = 0; y < h; ++y) {
+        const int ih = (int)(std::upper_bound(h0.begin(), h0.end(), y) - h0.begin()) - 1;
+        for (int iw = 0; iw < sw; ++iw) {
+          p->chunk_offsets.push_back(f * h * w + y * w + w0[iw]);
+          p->chunk_ranks.push_back(ih * sw + iw);
+        }
+      }
+    p->chunk_offsets.push_back(p->T);
+  } else if (mode == CPATTN_MODE_CONTIGUOUS) {
+    if (p->T < cp) return "contiguous split needs at least cp tokens";
+    const int64_t q = p->T / cp, rem = p->T % cp;
+    int64_t start = 0;
+    int s = 0;
+    for (int r = 0; r < cp; ++r) {
+      const int64_t len = q + (r < rem ? 1 : 0), end = start + len;
+      p->chunk_offsets.push_back(start);
+      p->chunk_ranks.push_back(r);
+      for (int64_t a = start; a < end;) {
+        while (cu[s + 1] <= a) ++s;
+        const int64_t b = std::min<int64_t>(end, cu[s + 1]);
+        p->rank_segments[r].push_back({a, b - a, s, a - cu[s]});
+        a = b;
+      }
+      start = end;
+    }
+    p->chunk_offsets.push_back(p->T);
+  } else {
+    return "unknown mode";
+  }
+  finish_common(p);
+  return std::string();
+}
+
+bool ring_entry(const cpattn_plan_t& p, int r, int t, bool causal, int32_t* kv_rank, int32_t* kind) {
+  const int cp = p.cp;
+  const int k = ((r - t) % cp + cp) % cp;
+  *kv_rank = k;
+  if (!causal) {
+    *kind = CPATTN_MASK_FULL;
+  } else if (k == r) {
+    *kind = CPATTN_MASK_DIAG;
+  } else if (p.mode == CPATTN_MODE_ZIGZAG) {
+    *kind = (k < r) ? CPATTN_MASK_KV_HEAD : CPATTN_MASK_Q_TAIL;
+  } else if (p.mode == CPATTN_MODE_CONTIGUOUS) {
+    *kind = (k < r) ? CPATTN_MASK_FULL : CPATTN_MASK_SKIP;
+  } else {
+    return false;
+  }
+  return true;
+}
+
+// Segments of `rank` that belong to sequence `seq` (segments are ordered by sequence).
+static std::pair<size_t, size_t> seq_range(const std::vector<Segment>& segs, int32_t seq) {
+  auto lo = std::lower_bound(segs.begin(), segs.end(), seq,
+                             [](const Segment& s, int32_t v) { return s.seq < v; });
+  auto hi = std::upper_bound(segs.begin(), segs.end(), seq,
+                             [](int32_t v, const Segment& s) { return v < s.seq; });
+  return {(size_t)(lo - segs.begin()), (size_t)(hi - segs.begin())};
+}
+
+static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool causal, int tile_m,
+                                                int tile_n, int q_rank, int step) {
+  auto wl = std::make_shared<WorkList>();
+  const int cp = p.cp;
+  const bool gathered = (p.mode == CPATTN_MODE_GRID2D);
+  // For GRID2D the kernel reads gathered shards: rank r's rows are the
+  // contiguous range [rank_offsets[r], rank_offsets[r+1]) of the gathered buffers.
+  auto segments_of = [&](int r) {
+    if (!gathered) return p.rank_segments[r];
+    std::vector<Segment> one;
+    const int64_t a = p.rank_offsets[r], b = p.rank_offsets[r + 1];
+    if (b > a) one.push_back({a, b - a, 0, a});
+    return one;
+  };
+  std::vector<std::vector<Segment>> segs(cp);
+  for (int r = 0; r < cp; ++r) segs[r] = segments_of(r);
+
+  const int r_lo = q_rank < 0 ? 0 : q_rank, r_hi = q_rank < 0 ? cp : q_rank + 1;
+  for (int r = r_lo; r < r_hi; ++r) {
+    int64_t local = 0;  // rank-local row of the current segment
+    for (const Segment& qs : segs[r]) {
+      for (int64_t off = 0; off < qs.len; off += tile_m) {
+        QTile t{};
+        const int64_t rows = std::min<int64_t>(tile_m, qs.len - off);
+        t.q_row0 = (int32_t)(qs.row0 + off);
+        t.q_pos0 = (int32_t)(qs.pos0 + off);
+        t.q_rows = (int32_t)rows;
+        t.rank = r;
+        if (q_rank >= 0)
+          t.out_row0 = (int32_t)(local + off);  // partial outputs: rank-local rows
+        else
+          t.out_row0 = t.q_row0;                // global rows (gathered rows for GRID2D)
+        t.run_begin = (int32_t)wl->runs.size();
+        const int64_t qp_first = qs.pos0 + off, qp_last = qp_first + rows - 1;
+        const int s_lo = q_rank < 0 ? 0 : step, s_hi = q_rank < 0 ? cp : step + 1;
+        int64_t ntiles = 0;
+        for (int st = s_lo; st < s_hi; ++st) {
+          const int k = ((r - st) % cp + cp) % cp;
+          const auto rng = seq_range(segs[k], qs.seq);
+          for (size_t i = rng.first; i < rng.second; ++i) {
+            const Segment& ks = segs[k][i];
+            KvRun run{};
+            run.kv_row0 = (int32_t)ks.row0;
+            run.kv_pos0 = (int32_t)ks.pos0;
+            int64_t len = ks.len;
+            run.causal = 0;
+            if (causal) {
+              if (ks.pos0 > qp_last) continue;                   // entirely in the future
+              if (ks.pos0 + ks.len - 1 > qp_first) {             // crosses the diagonal
+                len = std::min<int64_t>(ks.len, qp_last - ks.pos0 + 1);
+                run.causal = 1;
+              }
+            }
+            run.kv_len = (int32_t)len;
+            wl->runs.push_back(run);
+            ntiles += (len + tile_n - 1) / tile_n;
+          }
+        }
+        t.run_end = (int32_t)wl->runs.size();
+        t.n_kv_tiles = (int32_t)ntiles;
+        wl->total_kv_tiles += ntiles;
+        wl->tiles.push_back(t);
+      }
+      local += qs.len;
+    }
+  }
+  // Longest tiles first, so that the block scheduler's in-order dispatch
+  // finishes the heaviest work early (LPT order).
+  std::stable_sort(wl->tiles.begin(), wl->tiles.end(),
+                   [](const QTile& a, const QTile& b) { return a.n_kv_tiles > b.n_kv_tiles; });
+  return wl;
+}
+
+std::shared_ptr<const WorkList> get_worklist(cpattn_plan_t& p, bool causal, int tile_m, int tile_n,
+                                             int q_rank, int step) {
+  WorkKey key{causal ? 1 : 0, tile_m, tile_n, q_rank, step};
+  std::lock_guard<std::mutex> lock(p.mu);
+  auto it = p.cache.find(key);
+  if (it != p.cache.end()) return it->second;
+  auto wl = build_worklist(p, causal, tile_m, tile_n, q_rank, step);
+  p.cache[key] = wl;
+  return wl;
+}
+
+}  // namespace cpattn

@@ -1,0 +1,75 @@
+// Host planner: context-parallel splits, ring schedule and kernel work lists.
+#pragma once
+
+#include <cstdint>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/cpattn.h"
+#include "worklist.h"
+
+namespace cpattn {
+
+// A run of consecutive global rows of one sequence, owned by one rank.
+struct Segment {
+  int64_t row0;   // first row (global THD row, or gathered row for GRID2D work lists)
+  int64_t len;
+  int32_t seq;
+  int64_t pos0;   // position of row0 inside its sequence
+};
+
+struct WorkList {
+  std::vector<QTile> tiles;
+  std::vector<KvRun> runs;
+  int64_t total_kv_tiles = 0;
+};
+
+struct WorkKey {
+  int causal, tile_m, tile_n, q_rank, step;  // q_rank = -1: every rank, every step
+  bool operator<(const WorkKey& o) const {
+    return std::tie(causal, tile_m, tile_n, q_rank, step) <
+           std::tie(o.causal, o.tile_m, o.tile_n, o.q_rank, o.step);
+  }
+};
+
+}  // namespace cpattn
+
+struct cpattn_plan {
+  int32_t mode = 0;
+  int32_t cp = 1;
+  int32_t n_seqs = 0;
+  int64_t T = 0;
+  int32_t split_h = 0, split_w = 0;
+  std::vector<int32_t> cu;                 // [n+1]
+  std::vector<int64_t> chunk_offsets;      // [n_chunks+1]
+  std::vector<int32_t> chunk_ranks;        // [n_chunks]
+  std::vector<int64_t> rank_offsets;       // [cp+1]
+  std::vector<int32_t> local_cu;           // [cp*(n+1)]
+  std::vector<int64_t> index_map;          // [T]
+  std::vector<std::vector<cpattn::Segment>> rank_segments;  // per rank, local order
+
+  std::mutex mu;
+  std::map<cpattn::WorkKey, std::shared_ptr<const cpattn::WorkList>> cache;
+};
+
+namespace cpattn {
+
+// Returns an empty string on success, else the reason the inputs are invalid.
+std::string build_plan(const int32_t* cu, int32_t n_seqs, int32_t cp, int32_t mode,
+                       const int32_t* grid_fhw, cpattn_plan_t* out);
+
+void optimal_split(int32_t cp, int32_t* a, int32_t* b);
+
+// Ring schedule entry for (q rank r, step t).  Returns false for causal GRID2D.
+bool ring_entry(const cpattn_plan_t& p, int r, int t, bool causal, int32_t* kv_rank, int32_t* kind);
+
+// Work list of q tiles (tile_m rows) with their KV runs in ring order.
+// q_rank < 0: all ranks and all steps (whole forward); else one (rank, step).
+std::shared_ptr<const WorkList> get_worklist(cpattn_plan_t& p, bool causal, int tile_m, int tile_n,
+                                             int q_rank, int step);
+
+}  // namespace cpattn

@@ -1,0 +1,49 @@
+// Work-list records shared by the host planner and the attention kernels.
+//
+// A q tile is up to tile_m consecutive query rows of one sequence inside one
+// rank's shard.  Its KV runs list, in ring order, the key rows of the same
+// sequence that the tile's queries may see: at ring step t the q rank r reads
+// the shard of rank (r - t) mod cp, one run per contiguous piece of it.
+#pragma once
+
+#include <stdint.h>
+
+#define CPATTN_WS_HEADER_BYTES 256
+
+#ifdef __cplusplus
+namespace cpattn {
+#endif
+
+typedef struct QTile {
+  int32_t q_row0;     // row of the first query in the Q buffer
+  int32_t q_pos0;     // its position inside the sequence
+  int32_t out_row0;   // output row of the first query (global, rank-local or gathered)
+  int32_t q_rows;     // valid rows, 1..tile_m
+  int32_t run_begin;  // KV runs [run_begin, run_end)
+  int32_t run_end;
+  int32_t n_kv_tiles; // sum over runs of ceil(kv_len / tile_n)
+  int32_t rank;       // virtual rank that owns the tile
+} QTile;
+
+typedef struct KvRun {
+  int32_t kv_row0;    // row of the first key in the K/V buffers
+  int32_t kv_pos0;    // its position inside the sequence
+  int32_t kv_len;     // keys in the run (>= 1)
+  int32_t causal;     // 1: some key may follow some query of the tile (apply the position mask)
+} KvRun;
+
+// Fault word at the start of every workspace.
+typedef struct WsHeader {
+  uint32_t fault;     // 0 = none; else a CPATTN_FAULT_* code
+  uint32_t info;      // where (block index)
+  uint32_t detail;    // which wait / value
+  uint32_t pad[61];
+} WsHeader;
+
+#ifdef __cplusplus
+}  // namespace cpattn
+#endif
+
+#define CPATTN_FAULT_WAIT_TIMEOUT 1u
+#define CPATTN_FAULT_BAD_INDEX 2u
+#define CPATTN_FAULT_TMEM 3u

@@ -1,0 +1,269 @@
+/*
+ * cpattn - packed variable-length context-parallel attention on one GB300.
+ *
+ * C ABI of libcpattn.so.  Plain pointers and sizes only.
+ *
+ * Problem statement followed by this library:
+ *   - Packed THD inputs: variable-length sequences concatenated along T and
+ *     described by cu_seqlens ("Speeding up Variable-Length Training with
+ *     Dynamic Context Parallelism and NVIDIA Megatron Core", section on
+ *     dynamic rescheduling and packing, Fig. 1; PackedSeqParams carries
+ *     cu_seqlens and cp_size).
+ *   - A context-parallel (CP) group splits one sequence across ranks and runs
+ *     blockwise attention while KV blocks circulate in a ring ("Scaling video
+ *     training with parallelism", section 2, Ring Attention); the split is the
+ *     load-balanced zigzag of ZIGZAG-RINGATTN (LongVILA news article, Fig. 5,
+ *     Table 2) or a 2-D h x w tile grid (LongCat-Video context-parallel
+ *     article, tensor split strategy: split_tensor_in_cp_2d,
+ *     get_optimal_split, split_cp_2d / gather_cp_2d).
+ *   - Splitting must not change what the model computes ("Scaling video
+ *     training with parallelism", opening section): the merged result equals
+ *     plain softmax attention inside each packed sequence.
+ *   - Loss is normalised per valid token and FLOPs are counted from the real
+ *     sequence lengths (Dynamic-CP article, section "Loss computation and
+ *     FLOPS statistics").
+ * Every virtual CP rank is emulated on the one GPU: a ring step is a change
+ * of which KV rows a thread block reads next; no collective is issued.
+ *
+ * Conventions
+ *   - Layouts (row-major, contiguous):  Q [T,H,D], K and V [T,Hkv,D],
+ *     O [T,H,D] in the input dtype, LSE [H,T] fp32 (natural log, scale
+ *     included).  Query head h reads KV head floor(h*Hkv/H).
+ *   - Supported: dtype fp32 or bf16, D in {64, 128}, H % Hkv == 0,
+ *     1 <= H, Hkv <= 256, T < 2^31.  Anything else: CPATTN_UNSUPPORTED or
+ *     CPATTN_INVALID_ARG.  Device buffers must be 16-byte aligned.
+ *   - Every function returns a status and never aborts or exits.  The
+ *     message of the last failure on the calling thread is
+ *     cpattn_last_error_string().
+ *   - Device pointers are owned by the caller.  The library allocates no
+ *     device memory: functions that need scratch take a caller-provided
+ *     workspace of at least cpattn_workspace_size() bytes (256-byte aligned).
+ *     Plans are host objects owned by the library, freed with
+ *     cpattn_plan_destroy().
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device work
+ *     is asynchronous; argument errors are reported synchronously.  A kernel
+ *     that detects a fault (a bounded wait that ran out, a bad index) records
+ *     it in the workspace and returns early; cpattn_sync_status() reports it
+ *     as CPATTN_DEVICE_FAULT.
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cpattn_status {
+  CPATTN_OK = 0,
+  CPATTN_INVALID_ARG = 1,   /* bad pointer, size, cu_seqlens or plan input   */
+  CPATTN_UNSUPPORTED = 2,   /* valid request this build does not implement   */
+  CPATTN_WORKSPACE = 3,     /* workspace missing, misaligned or too small    */
+  CPATTN_CUDA_ERROR = 4,    /* a CUDA runtime/driver call failed             */
+  CPATTN_DEVICE_FAULT = 5   /* a kernel recorded a fault in the workspace    */
+} cpattn_status_t;
+
+typedef enum cpattn_mode {
+  CPATTN_MODE_ZIGZAG = 0,      /* 2*cp chunks per sequence, rank r owns r and 2cp-1-r */
+  CPATTN_MODE_GRID2D = 1,      /* one F x h x w latent cut into split_h x split_w tiles */
+  CPATTN_MODE_CONTIGUOUS = 2   /* packed T cut into cp contiguous ranges              */
+} cpattn_mode_t;
+
+typedef enum cpattn_dtype {
+  CPATTN_DTYPE_FP32 = 0,
+  CPATTN_DTYPE_BF16 = 1
+} cpattn_dtype_t;
+
+/* Which part of a (q rank, ring step) pair can interact under a causal mask. */
+typedef enum cpattn_mask_kind {
+  CPATTN_MASK_SKIP = 0,     /* nothing visible                                   */
+  CPATTN_MASK_FULL = 1,     /* every allowed pair (no causal cut inside the pair) */
+  CPATTN_MASK_DIAG = 2,     /* the rank's own shard: causal inside               */
+  CPATTN_MASK_KV_HEAD = 3,  /* zigzag, kv rank < q rank: the kv rank's first chunk only */
+  CPATTN_MASK_Q_TAIL = 4    /* zigzag, kv rank > q rank: the q rank's second chunk only */
+} cpattn_mask_kind_t;
+
+typedef struct cpattn_grid {
+  int32_t frames, height, width;   /* latent grid, tokens flattened (f, y, x) row-major */
+} cpattn_grid_t;
+
+typedef struct cpattn_plan cpattn_plan_t;
+
+typedef struct cpattn_plan_info {
+  int64_t total_tokens;     /* T = cu_seqlens[n_seqs]                            */
+  int64_t n_chunks;         /* contiguous global row runs the split cuts T into  */
+  int64_t max_rank_tokens;  /* largest per-rank shard                            */
+  int32_t n_seqs;
+  int32_t cp_size;
+  int32_t mode;             /* cpattn_mode_t                                     */
+  int32_t split_h;          /* GRID2D only, else 0                               */
+  int32_t split_w;          /* GRID2D only, else 0                               */
+  int32_t reserved;
+} cpattn_plan_info_t;
+
+/* ---------------------------------------------------------------- planning */
+
+/* Build the context-parallel split of a packed batch for `cp_size` virtual
+ * ranks.  Integer-only and deterministic.
+ *   cu_seqlens_host: host int32 [n_seqs+1], cu[0] = 0, strictly increasing.
+ *   ZIGZAG: sequence s (length L >= 2*cp) is cut into C = 2*cp chunks of
+ *     floor(L/C) + [j < L mod C] tokens; rank r owns chunks r and C-1-r
+ *     (zigzag ring split: LongVILA news article, Fig. 5 / Table 2).
+ *   GRID2D: n_seqs must be 1 and grid F*h*w must equal T.  (split_h, split_w)
+ *     is the factor pair of cp closest to square, the larger factor on the
+ *     larger side (tie: split_h <= split_w); sides are cut in pieces of
+ *     ceil(n/parts) with the remainder last; rank = ih*split_w + iw
+ *     (LongCat-Video article, tensor split strategy, get_optimal_split).
+ *   CONTIGUOUS: T cut into cp ranges, the first T mod cp one token longer
+ *     (token stage of MM-SP: "Scaling video training with parallelism",
+ *     section 3, Fig. 2).
+ *   grid: required for GRID2D, ignored otherwise (may be NULL).
+ *   out_plan: receives a plan owned by the caller until cpattn_plan_destroy.
+ * Errors: CPATTN_INVALID_ARG for cp_size < 1, bad cu_seqlens, a zigzag
+ * sequence shorter than 2*cp, a grid that does not match T or cannot be cut
+ * into the required pieces, or fewer tokens than ranks. */
+cpattn_status_t cpattn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t cp_size,
+                            cpattn_mode_t mode, const cpattn_grid_t* grid,
+                            cpattn_plan_t** out_plan);
+
+/* Free a plan (NULL is a no-op). */
+cpattn_status_t cpattn_plan_destroy(cpattn_plan_t* plan);
+
+/* Summary sizes of a plan. */
+cpattn_status_t cpattn_plan_get_info(const cpattn_plan_t* plan, cpattn_plan_info_t* out);
+
+/* Host copies of the plan's integer maps.  `n` is the capacity of `out` in
+ * elements; CPATTN_INVALID_ARG if it is smaller than required.
+ *   chunk_offsets [n_chunks+1]: global start row of each chunk, then T.
+ *     ZIGZAG chunk (s, j) is entry s*2cp + j; GRID2D chunks are the
+ *     (frame, row, w-piece) runs in global order; CONTIGUOUS chunk r is rank r.
+ *   chunk_ranks [n_chunks]: owning rank of each chunk.
+ *   rank_offsets [cp+1]: start of each rank's rows in the index map.
+ *   local_cu_seqlens [n_seqs+1] for `rank`: the rank's local rows per sequence.
+ *   index_map [T]: rank-major local row -> global row (zigzag local order is
+ *     chunk r then chunk 2cp-1-r of each sequence; grid tiles are (f, y, x)
+ *     row-major).
+ *   ring schedule [cp*cp] at index r*cp + t: the kv rank that q rank r works
+ *     with at ring step t, (r - t) mod cp ("Scaling video training with
+ *     parallelism", section 2, Ring Attention), and its cpattn_mask_kind_t
+ *     under `causal` (causal GRID2D plans: CPATTN_UNSUPPORTED). */
+cpattn_status_t cpattn_plan_get_chunk_offsets(const cpattn_plan_t* plan, int64_t* out, int64_t n);
+cpattn_status_t cpattn_plan_get_chunk_ranks(const cpattn_plan_t* plan, int32_t* out, int64_t n);
+cpattn_status_t cpattn_plan_get_rank_offsets(const cpattn_plan_t* plan, int64_t* out, int64_t n);
+cpattn_status_t cpattn_plan_get_local_cu_seqlens(const cpattn_plan_t* plan, int32_t rank,
+                                                 int32_t* out, int64_t n);
+cpattn_status_t cpattn_plan_get_index_map(const cpattn_plan_t* plan, int64_t* out, int64_t n);
+cpattn_status_t cpattn_plan_get_ring_schedule(const cpattn_plan_t* plan, int32_t causal,
+                                              int32_t* kv_rank, int32_t* mask_kind, int64_t n);
+
+/* ---------------------------------------------------------------- attention */
+
+/* Bytes of device workspace that cpattn_fwd / cpattn_block_fwd need for this
+ * plan and shape (work list, fault word and, for GRID2D, the gathered
+ * shards). */
+cpattn_status_t cpattn_workspace_size(const cpattn_plan_t* plan, int32_t H, int32_t Hkv, int32_t D,
+                                      cpattn_dtype_t dtype, int32_t causal, size_t* bytes);
+
+/* Whole packed forward: every virtual rank's query shard attends, ring step
+ * by ring step, to the KV shard it holds at that step; each step's partial is
+ * merged into the running result by exact log-sum-exp rescaling, and the
+ * final O/LSE are written at global THD rows.  Equals plain softmax attention
+ * inside each packed sequence (causal: key position <= query position).
+ *   q, k, v: device, layouts above, dtype `dtype`.
+ *   scale:   softmax scale (commonly 1/sqrt(D)).
+ *   o:       device [T,H,D] dtype;  lse: device [H,T] fp32.
+ *   workspace/ws_bytes: device scratch, >= cpattn_workspace_size().
+ * GRID2D gathers each rank's shard into the workspace first (split_cp_2d)
+ * and writes outputs back through the index map (gather_cp_2d).
+ * Causal GRID2D is CPATTN_UNSUPPORTED. */
+cpattn_status_t cpattn_fwd(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
+                           cpattn_dtype_t dtype, int32_t H, int32_t Hkv, int32_t D, float scale,
+                           int32_t causal, void* o, float* lse, void* workspace, size_t ws_bytes,
+                           void* stream);
+
+/* One ring step of one virtual rank: the attention of rank `q_rank`'s query
+ * shard over the KV shard of rank (q_rank - ring_step) mod cp, as a partial
+ * result normalised over that block ("Scaling video training with
+ * parallelism", section 2, Ring Attention: blockwise attention on local KV).
+ *   o_partial:   device fp32 [T_r,H,D], rows in rank-local order
+ *                (index_map[rank_offsets[q_rank] + i] is the global row of i).
+ *   lse_partial: device fp32 [H,T_r].
+ *   Rows with no allowed key in the block get O = 0 and lse = -inf.
+ * Merge the cp partials of a rank with cpattn_merge. */
+cpattn_status_t cpattn_block_fwd(const cpattn_plan_t* plan, const void* q, const void* k,
+                                 const void* v, cpattn_dtype_t dtype, int32_t H, int32_t Hkv,
+                                 int32_t D, float scale, int32_t causal, int32_t q_rank,
+                                 int32_t ring_step, float* o_partial, float* lse_partial,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
+/* Exact log-sum-exp merge of n partials of the same rows:
+ *   M = max_p lse_p;  lse = M + ln sum_p exp(lse_p - M);
+ *   O = sum_p exp(lse_p - lse) * O_p.
+ * Partials with lse = -inf contribute nothing; if all are -inf, O = 0 and
+ * lse = -inf.  (The pages name blockwise ring attention but not its merge;
+ * this is the identity that recombines softmax partials exactly.)
+ *   o_parts_host / lse_parts_host: host arrays of n_partials (1..64) device
+ *     pointers to fp32 [rows,H,D] and fp32 [H,rows].
+ *   out_rows: device int64 [rows] giving the output row of each input row,
+ *     or NULL for the identity; out_total_rows is the row count of o_out and
+ *     the leading dimension of lse_out ([H,out_total_rows]).
+ *   o_out: device [out_total_rows,H,D] of out_dtype; lse_out: device fp32. */
+cpattn_status_t cpattn_merge(int32_t n_partials, const float* const* o_parts_host,
+                             const float* const* lse_parts_host, int64_t rows, int32_t H,
+                             int32_t D, const int64_t* out_rows, int64_t out_total_rows,
+                             void* o_out, cpattn_dtype_t out_dtype, float* lse_out, void* stream);
+
+/* Row permutation between global THD order and rank shards (the local
+ * equivalents of split_cp_2d and gather_cp_2d, LongCat-Video article,
+ * communication primitives).  `index` is device int64 [rows]:
+ *   gather:  dst[i] = src[index[i]]   (global -> shard order); src has src_rows rows
+ *   scatter: dst[index[i]] = src[i]   (shard -> global order); dst has dst_rows rows
+ * A row whose index lies outside [0, src_rows) / [0, dst_rows) is skipped.
+ * Each row is row_bytes bytes (a multiple of 16); buffers are 16-byte
+ * aligned and must not overlap. */
+cpattn_status_t cpattn_gather_rows(const void* src, int64_t src_rows, void* dst, const int64_t* index,
+                                   int64_t rows, int64_t row_bytes, void* stream);
+cpattn_status_t cpattn_scatter_rows(const void* src, void* dst, int64_t dst_rows, const int64_t* index,
+                                    int64_t rows, int64_t row_bytes, void* stream);
+
+/* --------------------------------------------------------------- loss, FLOPs */
+
+/* Per-token loss normalisation over valid tokens (Dynamic-CP article, section
+ * "Loss computation and FLOPS statistics"):
+ *   *out_loss = sum_t [valid_t != 0] loss_t / sum_t [valid_t != 0]
+ * accumulated in fp64 in a fixed order (deterministic), *out_count the exact
+ * number of valid tokens.  With no valid token *out_loss = 0.
+ *   loss: device fp32 [T]; valid: device uint8 [T] (0 = padding).
+ *   out_loss: device fp64 scalar; out_count: device int64 scalar;
+ *   out_loss_f32: device fp32 scalar or NULL. */
+cpattn_status_t cpattn_token_loss_norm(const float* loss, const uint8_t* valid, int64_t T,
+                                       double* out_loss, int64_t* out_count, float* out_loss_f32,
+                                       void* stream);
+
+/* THD-aware forward FLOPs, 4*D*H*sum_s pairs(L_s), pairs = L(L+1)/2 causal,
+ * L^2 otherwise; counted from the real lengths, never max_seqlen (Dynamic-CP
+ * article, section "Loss computation and FLOPS statistics").  Exact integer
+ * in *out_u64 (may be NULL), the same as a double in *out_f64 (may be NULL). */
+cpattn_status_t cpattn_fwd_flops(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t H,
+                                 int32_t D, int32_t causal, uint64_t* out_u64, double* out_f64);
+
+/* ----------------------------------------------------------------- helpers */
+
+/* Synchronise `stream`, then report a fault recorded by a kernel in
+ * `workspace` (CPATTN_DEVICE_FAULT) or a CUDA error (CPATTN_CUDA_ERROR).
+ * The fault word is cleared by the next cpattn_fwd / cpattn_block_fwd. */
+cpattn_status_t cpattn_sync_status(const void* workspace, void* stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* cpattn_last_error_string(void);
+
+/* Library version string. */
+const char* cpattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H */

@@ -139,8 +139,10 @@ def attention_at_rows(q, k, v, cu_seqlens, rows, causal: bool, scale: float,
     Used at sizes where the whole output is too large for the CPU: each
     sampled row is still computed from its full definition.  ``q`` may be the
     full [T,H,D] tensor; ``k``/``v`` are full [T,Hkv,D] tensors (torch or
-    numpy, any float dtype).  KV heads are converted to fp64 one at a time;
-    independent row batches run on a thread pool (numpy releases the GIL).
+    numpy, any float dtype).  For each KV head and each sequence holding a
+    sampled row, the keys up to the last sampled row are converted to fp64
+    once; independent row batches run on a thread pool (numpy releases the
+    GIL).
     """
     rows = np.asarray(rows, dtype=np.int64)
     cu = np.asarray(cu_seqlens, dtype=np.int64)
@@ -157,32 +159,29 @@ def attention_at_rows(q, k, v, cu_seqlens, rows, causal: bool, scale: float,
     for g in range(Hkv):
         heads = [h for h in range(H) if kv_head(h, H, Hkv) == g]
         assert len(heads) == G
-        k_g = to_f64(k[:, g, :])
-        v_g = to_f64(v[:, g, :])
-        # batches of rows from the same sequence
-        jobs = []
         for s in np.unique(seq):
-            idx = np.nonzero(seq == s)[0]
-            for b0 in range(0, len(idx), batch):
-                jobs.append((int(s), idx[b0:b0 + batch]))
-
-        def work(job):
-            s, idx = job
+            idx_s = np.nonzero(seq == s)[0]
             a, b = int(cu[s]), int(cu[s + 1])
-            rr = rows[idx]
-            kend = int(rr.max()) + 1 if causal else b
-            Qb = qr[idx][:, heads, :].reshape(len(idx) * G, D)
-            S = scale * (Qb @ k_g[a:kend].T)
-            if causal:
-                qpos = np.repeat(rr - a, G)[:, None]
-                kpos = np.arange(kend - a)[None, :]
-                S = np.where(causal_visible(kpos, qpos), S, -np.inf)
-            Ob, Lb = _softmax_rows(S, v_g[a:kend])
-            return idx, Ob.reshape(len(idx), G, D), Lb.reshape(len(idx), G)
+            kend_s = int(rows[idx_s].max()) + 1 if causal else b
+            k_s = to_f64(k[a:kend_s, g, :])   # keys of this sequence up to the last sampled row
+            v_s = to_f64(v[a:kend_s, g, :])
 
-        with ThreadPoolExecutor(max_workers=threads) as ex:
-            for idx, Ob, Lb in ex.map(work, jobs):
-                for gi, h in enumerate(heads):
-                    O[idx, h, :] = Ob[:, gi, :]
-                    LSE[h, idx] = Lb[:, gi]
+            def work(idx, a=a, b=b, k_s=k_s, v_s=v_s):
+                rr = rows[idx]
+                kend = int(rr.max()) + 1 if causal else b
+                Qb = qr[idx][:, heads, :].reshape(len(idx) * G, D)
+                S = scale * (Qb @ k_s[: kend - a].T)
+                if causal:
+                    qpos = np.repeat(rr - a, G)[:, None]
+                    kpos = np.arange(kend - a)[None, :]
+                    S = np.where(causal_visible(kpos, qpos), S, -np.inf)
+                Ob, Lb = _softmax_rows(S, v_s[: kend - a])
+                return idx, Ob.reshape(len(idx), G, D), Lb.reshape(len(idx), G)
+
+            batches = [idx_s[i:i + batch] for i in range(0, len(idx_s), batch)]
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                for idx, Ob, Lb in ex.map(work, batches):
+                    for gi, h in enumerate(heads):
+                        O[idx, h, :] = Ob[:, gi, :]
+                        LSE[h, idx] = Lb[:, gi]
     return O, LSE

@@ -11,3 +11,12 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+@pytest.fixture(scope="session")
+def cpattn():
+    """The library binding, built in-tree (nvcc cross-compiles without a GPU)."""
+    import context_attention_cpattn_gb300 as m
+    m.build()
+    m.lib()
+    return m

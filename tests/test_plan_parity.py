@@ -1,0 +1,60 @@
+"""The library's planner (C++) matches the oracle's independent restatement
+bit for bit: chunk table, owners, rank offsets, local cu_seqlens, index map
+and ring schedule."""
+
+import numpy as np
+import pytest
+
+import inputs
+from oracle import plan as P
+
+
+def _compare(cpattn, cu, cp, mode, grid=None):
+    ref = P.make_plan(cu, cp, mode, grid)
+    got = cpattn.cpattn_plan(cu, cp, mode, grid)
+    info = got.info()
+    assert info["total_tokens"] == ref.T
+    assert info["n_chunks"] == len(ref.chunk_ranks)
+    assert (info["split_h"], info["split_w"]) == (ref.split_h, ref.split_w)
+    assert np.array_equal(got.chunk_offsets(), ref.chunk_offsets)
+    assert np.array_equal(got.chunk_ranks(), ref.chunk_ranks)
+    assert np.array_equal(got.rank_offsets(), ref.rank_offsets)
+    assert np.array_equal(got.index_map(), ref.index_map)
+    for r in range(cp):
+        assert np.array_equal(got.local_cu_seqlens(r), ref.local_cu_seqlens[r])
+    for causal in ((False,) if P.MODES.get(mode, mode) == P.GRID2D else (False, True)):
+        kv, kind = got.ring_schedule(causal)
+        rkv, rkind = P.ring_schedule(ref, causal)
+        assert np.array_equal(kv, rkv) and np.array_equal(kind, rkind)
+
+
+@pytest.mark.parametrize("name", ["tiny_packed_fp32", "dynamic_cp_microbatch", "long_video_200k_gqa",
+                                  "video_latent_grid2d"])
+def test_workload_plans_match_oracle(cpattn, name):
+    w = inputs.workload(name)
+    _compare(cpattn, w.cu_seqlens, w.cp, w.mode, w.grid)
+
+
+@pytest.mark.slow
+def test_million_token_plan_matches_oracle(cpattn):
+    w = inputs.workload("single_seq_1m_gqa")
+    _compare(cpattn, w.cu_seqlens, w.cp, w.mode)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_plans_match_oracle(cpattn, seed):
+    rng = np.random.default_rng(seed)
+    for cp in (1, 2, 3, 4, 8):
+        lens = rng.integers(2 * cp, 300, size=rng.integers(1, 7))
+        cu = np.concatenate([[0], np.cumsum(lens)])
+        _compare(cpattn, cu, cp, "zigzag")
+        _compare(cpattn, cu, cp, "contiguous")
+    for cp in (1, 2, 4, 6, 8):
+        F, h, w = rng.integers(1, 4), rng.integers(4, 20), rng.integers(4, 20)
+        try:
+            ref = P.grid2d((0, F * h * w), cp, (F, h, w))
+        except P.PlanError:
+            with pytest.raises(cpattn.CpattnError):
+                cpattn.cpattn_plan([0, F * h * w], cp, "grid2d", (F, h, w))
+            continue
+        _compare(cpattn, (0, F * h * w), cp, "grid2d", (F, h, w))
