@@ -1,0 +1,74 @@
+"""Host logic of bench.py: replica barrier and max-over-ranks (gloo, world
+size 2, CPU), the nvidia-smi clock summary, and the reference arm's rank
+handling."""
+
+import json
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out_dir):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    rep = bench.Replicas(backend="gloo")
+    rep.barrier()
+    m = rep.max(10.0 + rank)          # each rank's elapsed time; all ranks see the slowest
+    rep.barrier()
+    with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+        json.dump({"rank": rep.rank, "world": rep.world, "max": m}, f)
+    rep.close()
+
+
+def test_replicas_barrier_and_max_over_two_gloo_ranks(tmp_path):
+    port = _free_port()
+    mp.start_processes(_worker, args=(2, port, str(tmp_path)), nprocs=2, join=True, start_method="spawn")
+    res = [json.load(open(tmp_path / f"r{r}.json")) for r in range(2)]
+    assert [r["rank"] for r in res] == [0, 1]
+    assert all(r["world"] == 2 and r["max"] == 11.0 for r in res)
+
+
+def test_single_process_replicas_are_trivial(monkeypatch):
+    for v in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(v, raising=False)
+    rep = bench.Replicas()
+    assert rep.world == 1 and rep.max(3.5) == 3.5
+    rep.barrier()
+
+
+def test_clock_summary():
+    text = "\n".join([
+        "0, 345, 2070, 200.5, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1890, 2070, 1100.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 1905, 2070, 1150.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 1920, 2070, 1170.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ])
+    c = bench.summarise_clocks(text)
+    assert c["sm_max_mhz"] == 2070 and c["sm_mhz"] == 1905 and c["reasons"] == ["sw_power_cap"]
+    assert bench.summarise_clocks("") is None
+
+
+def test_reference_arm_non_zero_rank_does_nothing(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"])
+    assert capsys.readouterr().out == ""
+
+
+def test_row_flops_counts_real_lengths():
+    import numpy as np
+    cu = [0, 10, 30]
+    rows = np.array([0, 9, 10, 29])
+    assert bench.row_flops(cu, rows, 2, 4, True) == 4 * 4 * 2 * (1 + 10 + 1 + 20)
+    assert bench.row_flops(cu, rows, 2, 4, False) == 4 * 4 * 2 * (10 + 10 + 20 + 20)
