@@ -59,6 +59,7 @@ _SIGNATURES = {
     "cpattn_plan_get_ring_schedule": [_P, _I32, _P, _P, _I64],
     "cpattn_workspace_size": [_P, _I32, _I32, _I32, _I32, _I32, _P],
     "cpattn_fwd": [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _I32, _P, _P, _P, _SZ, _P],
+    "cpattn_fwd_static": [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _I32, _P, _P, _P],
     "cpattn_block_fwd": [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P],
     "cpattn_merge": [_I32, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _I32, _P, _P],
     "cpattn_gather_rows": [_P, _I64, _P, _P, _I64, _I64, _P],
@@ -220,6 +221,19 @@ def cpattn_fwd(plan: Plan, q, k, v, o, lse, workspace, scale: Optional[float] = 
     _check(lib().cpattn_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), H, Hkv, D, scale,
                             int(bool(causal)), _ptr(o), _ptr(lse), _ptr(workspace), workspace.numel(),
                             _stream(stream)))
+
+
+def cpattn_fwd_static(plan: Plan, q, k, v, o, lse, scale: Optional[float] = None, causal: bool = True,
+                      stream=None):
+    """cpattn_fwd without a workspace, for callers that cannot allocate device
+    memory: the scratch is a fixed 8 MiB array inside the library, shared by
+    every call (serialise calls; make the first call on a device before any
+    stream capture)."""
+    T, H, D = q.shape
+    Hkv = k.shape[1]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    _check(lib().cpattn_fwd_static(plan.handle, _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), H, Hkv, D, scale,
+                                   int(bool(causal)), _ptr(o), _ptr(lse), _stream(stream)))
 
 
 def cpattn_block_fwd(plan: Plan, q, k, v, o_partial, lse_partial, workspace, q_rank: int, ring_step: int,

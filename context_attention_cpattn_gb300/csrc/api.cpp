@@ -179,6 +179,12 @@ cpattn_status_t prepare(const cpattn_plan_t* plan, const void* q, const void* k,
 
 }  // namespace
 
+namespace cpattn {
+// Records the message of a failure for cpattn_last_error_string (used by
+// entry points defined in other translation units).
+cpattn_status_t set_error(cpattn_status_t s, const std::string& msg) { return fail(s, msg); }
+}  // namespace cpattn
+
 extern "C" {
 
 cpattn_status_t cpattn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t cp_size, cpattn_mode_t mode,

@@ -228,6 +228,37 @@ cpattn_status_t cpattn_gather_rows(const void* src, int64_t src_rows, void* dst,
 cpattn_status_t cpattn_scatter_rows(const void* src, void* dst, int64_t dst_rows, const int64_t* index,
                                     int64_t rows, int64_t row_bytes, void* stream);
 
+/* Bytes of device scratch compiled into the library for cpattn_fwd_static. */
+#define CPATTN_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* The packed forward of cpattn_fwd for callers that cannot allocate device
+ * memory: a plugin or operator interface that passes only input and output
+ * buffers, or a process whose device memory belongs entirely to another
+ * allocator.  (The pages have no counterpart: this is an interface
+ * convenience, not a step of the method.)
+ *   Same arguments and results as cpattn_fwd, without the workspace.  The
+ *   call allocates no device or pinned host memory: its scratch (fault word
+ *   and work list) is a fixed array of CPATTN_STATIC_SCRATCH_BYTES (8 MiB)
+ *   inside the library, held on every GPU that loads the library until the
+ *   process exits.
+ *   The first call on each device finds the array's device address with
+ *   cudaGetSymbolAddress (that device must be current); make that first call
+ *   before any stream capture.
+ *   Every call shares the one array and it keeps the last call's contents
+ *   (each call clears the fault word and rewrites the work list), so calls
+ *   that overlap on the GPU - on different streams, or from different
+ *   threads - race: serialise them.
+ *   The work list is copied from pageable host memory, so the call waits for
+ *   work already queued on `stream` before it returns.
+ *   Errors: CPATTN_WORKSPACE when the plan's work list does not fit in the
+ *   array (the message gives both sizes); CPATTN_UNSUPPORTED for GRID2D plans,
+ *   whose shard gather needs more scratch than the array holds.  A fault that
+ *   a kernel records in the array's fault word is not reported by
+ *   cpattn_sync_status. */
+cpattn_status_t cpattn_fwd_static(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
+                                  cpattn_dtype_t dtype, int32_t H, int32_t Hkv, int32_t D, float scale,
+                                  int32_t causal, void* o, float* lse, void* stream);
+
 /* --------------------------------------------------------------- loss, FLOPs */
 
 /* Per-token loss normalisation over valid tokens (Dynamic-CP article, section

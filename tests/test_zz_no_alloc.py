@@ -1,0 +1,82 @@
+"""cpattn_fwd_static, the forward for callers that cannot allocate device
+memory (a plugin interface that passes only input and output buffers, or a
+process whose device memory another allocator owns), gives the results of the
+workspace forward cpattn_fwd on two calls in a row.
+
+This file is collected last on purpose: a run that stops at the first failure
+has run every other test before it.  It also passes alone in a fresh process.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import inputs
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cp():
+    import context_attention_cpattn_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    m.build()
+    m.lib()
+    return m
+
+
+def _workspace_forward(cp, plan, w, qd, kd, vd):
+    return U.run_fwd(cp, plan, w, qd, kd, vd)
+
+
+def _static_forward(cp, plan, w, qd, kd, vd):
+    """Through the C ABI directly: no workspace argument at all."""
+    T, H, D = qd.shape
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full((H, T), float("nan"), dtype=torch.float32, device="cuda")
+    L = cp.lib()
+    dt = cp.DTYPE_BF16 if qd.dtype == torch.bfloat16 else cp.DTYPE_FP32
+    s = L.cpattn_fwd_static(plan.handle, ctypes.c_void_p(qd.data_ptr()), ctypes.c_void_p(kd.data_ptr()),
+                            ctypes.c_void_p(vd.data_ptr()), dt, H, kd.shape[1], D, w.scale, int(w.causal),
+                            ctypes.c_void_p(o.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert s == cp.OK, L.cpattn_last_error_string()
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def _compare(got, ref, dtype, where):
+    o, lse = got
+    o_ref, lse_ref = ref
+    U.check(o, lse, o_ref.to("cpu", torch.float64).numpy(), lse_ref.to("cpu", torch.float64).numpy(), dtype, where)
+
+
+def test_static_scratch_forward_matches_workspace_forward(cp):
+    cases = [inputs.workload("dynamic_cp_microbatch"), inputs.workload("tiny_packed_fp32"),
+             inputs.custom((0, 300, 557), 8, 2, 128, dtype="bf16", causal=True, mode="contiguous", cp=3)]
+    for w in cases:
+        (q, k, v), (qd, kd, vd) = U.device_inputs(w)
+        plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode)
+        ref = _workspace_forward(cp, plan, w, qd, kd, vd)
+        first = _static_forward(cp, plan, w, qd, kd, vd)
+        second = _static_forward(cp, plan, w, qd, kd, vd)   # the scratch still holds the first call's list
+        _compare(first, ref, w.dtype, f"{w.name} first call")
+        _compare(second, ref, w.dtype, f"{w.name} second call")
+        assert not torch.isnan(second[0]).any()
+
+
+def test_static_scratch_rejects_what_it_cannot_hold(cp):
+    L = cp.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    grid = cp.cpattn_plan([0, 2 * 9 * 20], 4, "grid2d", (2, 9, 20))
+    s = L.cpattn_fwd_static(grid.handle, fake, fake, fake, cp.DTYPE_BF16, 2, 2, 128, 0.1, 0, fake, fake, None)
+    assert s == cp.UNSUPPORTED
+    # many short sequences with a large cp: the work list outgrows the 8 MiB array
+    big = cp.cpattn_plan(np.arange(0, 64 * 2001, 64), 32, "zigzag")
+    s = L.cpattn_fwd_static(big.handle, fake, fake, fake, cp.DTYPE_BF16, 2, 2, 128, 0.1, 1, fake, fake, None)
+    assert s == cp.WORKSPACE
+    assert b"static scratch holds" in L.cpattn_last_error_string()
