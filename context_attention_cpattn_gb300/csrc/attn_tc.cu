@@ -9,28 +9,38 @@
 // rescaling, so each ring step's partial (O_t, lse_t) is folded in as soon as
 // it is produced and never leaves the SM.
 //
+// Two blocks share each SM (about 97 KB of shared memory and 256 TMEM
+// columns each), so one block's softmax, prologue and epilogue overlap the
+// other block's matrix multiplies.
+//
 // Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K and V tiles through NS-deep rings
-//               (K one tile ahead of V, matching the order they are consumed).
-//   warp 1      TMEM allocator and MMA issuer (one thread):
-//                 S_j = Q K_j^T   (M=128, N=128, K=D)   into TMEM S[j%2]
-//                 O  += P_j V_j   (M=128, N=D,   K=128) into TMEM O
-//               S_{j+1} is issued before PV_j so the tensor core computes the
-//               next scores while the softmax warps work on this tile.
+//   warp 0      TMA producer: Q once, then K_j and V_j into single buffers;
+//               K_{j+1} is loaded as soon as S_j = Q K_j^T has consumed K_j,
+//               V_{j+1} as soon as O += P_j V_j has consumed V_j.
+//   warp 1      TMEM allocator and MMA issuer (one thread), in order:
+//                 S_0, PV_0, S_1, PV_1, ...
+//                 S_j  = Q K_j^T  (M=128, N=128, K=D)   A, B from shared memory
+//                 O   += P_j V_j  (M=128, N=D,   K=128) A = P from TMEM, B = V
+//               P_j lives in TMEM over the columns of S_j; S_{j+1} is issued
+//               after PV_j, and tcgen05.mma ops from one thread run in issue
+//               order, so PV_j has read P_j before S_{j+1} overwrites it.
 //   warps 2-5   softmax + epilogue, one query row per thread: read S from
 //               TMEM, apply the causal / run-end mask from token positions,
-//               update the running max and sum, write P (bf16) to shared
-//               memory in the 128-byte-swizzled K-major layout the MMA reads,
-//               and rescale O in TMEM when the running max moves by more than
-//               2^8 (otherwise the stale max is kept: O and the sum share it,
-//               so the final O/l is exact).
+//               update the running max and sum, write P (bf16 pairs) back to
+//               TMEM, and rescale O in TMEM when the running max grows by more
+//               than 2^8 (otherwise the stale max is kept: O and the sum share
+//               it, so the final O/l is exact).  When S_j has landed, every
+//               earlier MMA - PV_{j-1} included - has finished, so O may be
+//               rescaled without a further wait.
 //
-// Shared-memory operand layouts (all 1024-byte aligned, SWIZZLE_128B):
+// Shared-memory operand layouts (1024-byte aligned, SWIZZLE_128B):
 //   Q, K: [128 rows][64 columns] boxes, K-major (rows = M or N, columns = K).
 //   V:    [128 keys][64 d] boxes; as the B operand of P.V (N = d, K = keys)
 //         this is MN-major: 8-key groups 1024 B apart (SBO), 64-wide d
 //         blocks one box apart (LBO).
-//   P:    [128 rows][64 keys] x 2 boxes, K-major, written by the softmax warps.
+// Dispatch order: blocks of one KV head (all its query heads, every query
+// tile longest-first) are consecutive, so the KV rows the resident blocks
+// stream stay in L2.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -54,6 +64,7 @@ struct alignas(64) TcParams {
   const int64_t* out_map;
   WsHeader* ws;
   int64_t lse_ld;
+  int32_t n_tiles;
   int32_t H, Hkv;
   float scale;        // softmax scale (natural-log domain)
   float scale_log2;   // scale * log2(e)
@@ -63,18 +74,16 @@ struct alignas(64) TcParams {
 template <int D>
 struct TcCfg {
   static constexpr int KB = D / 64;                 // 64-column boxes per row
-  static constexpr int NS = (D == 128) ? 2 : 4;     // K and V ring depth
   static constexpr uint32_t BOX = 128 * 128;        // 128 rows x 128 bytes
   static constexpr uint32_t Q_BYTES = KB * BOX;
   static constexpr uint32_t KV_BYTES = KB * BOX;
   static constexpr uint32_t OFF_K = Q_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + NS * KV_BYTES;
-  static constexpr uint32_t OFF_P = OFF_V + NS * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_P + 2 * BOX;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;
+  static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + KV_BYTES;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 128;
   static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
-  static constexpr uint32_t TMEM_COLS = 512;              // S0 | S1 | O
-  static constexpr uint32_t TM_S = 0, TM_O = 256;
+  static constexpr uint32_t TMEM_COLS = 256;              // S (P aliased) | O
+  static constexpr uint32_t TM_S = 0, TM_O = 128;
 };
 
 // Advances through the KV runs of a q tile in 128-key steps.
@@ -90,9 +99,8 @@ struct KvCursor {
 };
 
 template <int D, bool kPartial>
-__global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<D>;
-  constexpr int NS = C::NS;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
 
@@ -100,39 +108,37 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = q_full + 1;
-  uint64_t* k_empty = k_full + NS;
-  uint64_t* v_full = k_empty + NS;
-  uint64_t* v_empty = v_full + NS;
-  uint64_t* s_full = v_empty + NS;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* drain = o_done + 1;
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = bars + 2;
+  uint64_t* v_full = bars + 3;
+  uint64_t* v_empty = bars + 4;
+  uint64_t* s_full = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* o_done = bars + 7;
+  uint64_t* drain = bars + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);  // [0] K loads, [1] V loads, [2] Q
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_id = blockIdx.x / p.H;
-  const int h = blockIdx.x - tile_id * p.H;
-  const int g = h / (p.H / p.Hkv);
+  // block -> (KV head g, query tile, query head inside the group)
+  const int G = p.H / p.Hkv;
+  const int hq = blockIdx.x % G;
+  const int rest = blockIdx.x / G;
+  const int tile_id = rest % p.n_tiles;
+  const int g = rest / p.n_tiles;
+  const int h = g * G + hq;
   const QTile tile = p.tiles[tile_id];
   const int n_kv = tile.n_kv_tiles;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(k_full + i, 1);
-      mbar_init(k_empty + i, 1);
-      mbar_init(v_full + i, 1);
-      mbar_init(v_empty + i, 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(s_full + i, 1);
-      mbar_init(s_free + i, 128);
-    }
+    mbar_init(k_full, 1);
+    mbar_init(k_empty, 1);
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
+    mbar_init(s_full, 1);
     mbar_init(p_full, 128);
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
@@ -160,77 +166,60 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
       for (int kb = 0; kb < C::KB; ++kb)
         tma_load_3d(smem + kb * C::BOX, &p.tm_q, q_full, kb * 64, h, tile.q_row0);
       issued[2] = 1;
-      KvCursor ck{tile.run_begin, 0}, cv{tile.run_begin, 0};
-      int jk = 0, jv = 0;
-      while (jk < n_kv || jv < n_kv) {
-        if (jk < n_kv && jk <= jv + 1) {
-          const int st = jk % NS;
-          if (jk >= NS && !wait_bounded(k_empty + st, ((jk / NS) - 1) & 1, abort_flag, p.ws, 1)) break;
-          const int row = p.runs[ck.r].kv_row0 + ck.off;
-          mbar_arrive_expect_tx(k_full + st, C::KV_BYTES);
-          uint8_t* dst = smem + C::OFF_K + st * C::KV_BYTES;
-          for (int kb = 0; kb < C::KB; ++kb) tma_load_3d(dst + kb * C::BOX, &p.tm_k, k_full + st, kb * 64, g, row);
-          ck.next(p.runs);
-          issued[0] = ++jk;
-        } else {
-          const int st = jv % NS;
-          if (jv >= NS && !wait_bounded(v_empty + st, ((jv / NS) - 1) & 1, abort_flag, p.ws, 2)) break;
-          const int row = p.runs[cv.r].kv_row0 + cv.off;
-          mbar_arrive_expect_tx(v_full + st, C::KV_BYTES);
-          uint8_t* dst = smem + C::OFF_V + st * C::KV_BYTES;
-          for (int kb = 0; kb < C::KB; ++kb) tma_load_3d(dst + kb * C::BOX, &p.tm_v, v_full + st, kb * 64, g, row);
-          cv.next(p.runs);
-          issued[1] = ++jv;
-        }
+      KvCursor c{tile.run_begin, 0};
+      for (int j = 0; j < n_kv; ++j) {
+        const int row = p.runs[c.r].kv_row0 + c.off;
+        if (j > 0 && !wait_bounded(k_empty, (j - 1) & 1, abort_flag, p.ws, 1)) break;
+        mbar_arrive_expect_tx(k_full, C::KV_BYTES);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(smem + C::OFF_K + kb * C::BOX, &p.tm_k, k_full, kb * 64, g, row);
+        issued[0] = j + 1;
+        if (j > 0 && !wait_bounded(v_empty, (j - 1) & 1, abort_flag, p.ws, 2)) break;
+        mbar_arrive_expect_tx(v_full, C::KV_BYTES);
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_3d(smem + C::OFF_V + kb * C::BOX, &p.tm_v, v_full, kb * 64, g, row);
+        issued[1] = j + 1;
+        c.next(p.runs);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_kv > 0) {
-      const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + C::OFF_K);
-      const uint32_t sV = smem_u32(smem + C::OFF_V), sP = smem_u32(smem + C::OFF_P);
-      auto issue_s = [&](int i) {
-        const uint32_t d = tmem + C::TM_S + 128u * (i & 1);
-        const uint32_t kbase = sK + (i % NS) * C::KV_BYTES;
+      const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      auto issue_s = [&]() {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::BOX + (kk & 3) * 32;
-          umma_bf16_ss(d, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(kbase + off, 16, 1024), IDESC_S,
-                       kk > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + C::TM_S, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
+                       IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
       bool ok = wait_bounded(q_full, 0, abort_flag, p.ws, 3) && wait_bounded(k_full, 0, abort_flag, p.ws, 4);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
-        if (NS < n_kv) umma_commit(k_empty);
+        issue_s();
+        if (n_kv > 1) umma_commit(k_empty);
         umma_commit(s_full);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          const int i = j + 1, st = i % NS;
-          ok = wait_bounded(k_full + st, (i / NS) & 1, abort_flag, p.ws, 5);
-          if (ok && i >= 2) ok = wait_bounded(s_free + (i & 1), ((i >> 1) - 1) & 1, abort_flag, p.ws, 6);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(i);
-          if (i + NS < n_kv) umma_commit(k_empty + st);
-          umma_commit(s_full + (i & 1));
-        }
-        ok = wait_bounded(p_full, j & 1, abort_flag, p.ws, 7) &&
-             wait_bounded(v_full + (j % NS), (j / NS) & 1, abort_flag, p.ws, 8);
+        ok = wait_bounded(p_full, j & 1, abort_flag, p.ws, 5) && wait_bounded(v_full, j & 1, abort_flag, p.ws, 6);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t vbase = sV + (j % NS) * C::KV_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * C::BOX + (kk & 3) * 32;  // P: 16 keys inside a 64-key box
-          const uint32_t boff = kk * 2048;                          // V: 16 keys = two 8-row groups
-          umma_bf16_ss(tmem + C::TM_O, smem_desc_sw128(sP + aoff, 16, 1024),
-                       smem_desc_sw128(vbase + boff, C::BOX, 1024), IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA: P columns 8kk.., V rows 16kk..
+          umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 8 * kk, smem_desc_sw128(sV + kk * 2048, C::BOX, 1024),
+                       IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+        if (j + 1 < n_kv) {
+          umma_commit(v_empty);
+          ok = wait_bounded(k_full, (j + 1) & 1, abort_flag, p.ws, 7);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s();
+          if (j + 2 < n_kv) umma_commit(k_empty);
+          umma_commit(s_full);
+        } else {
+          umma_commit(o_done);
         }
-        if (j + NS < n_kv) umma_commit(v_empty + (j % NS));
-        umma_commit(o_done);
       }
     }
   } else {
@@ -238,7 +227,6 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-    const uint32_t sP = smem_u32(smem + C::OFF_P);
     const int q_pos = tile.q_pos0 + row;
     const float c2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
@@ -251,15 +239,13 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
       const bool tile_mask = (n_keys < 128) || (run.causal && kpos0 + n_keys - 1 > tile.q_pos0);
       cur.next(p.runs);
 
-      if (!__all_sync(0xffffffffu, wait_bounded(s_full + (j & 1), (j >> 1) & 1, abort_flag, p.ws, 9))) {
+      if (!__all_sync(0xffffffffu, wait_bounded(s_full, j & 1, abort_flag, p.ws, 9))) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[128];
-      tmem_ld128_wait(tl + C::TM_S + 128u * (j & 1), sr);
-      tc_fence_before();
-      mbar_arrive(s_free + (j & 1));
+      tmem_ld128_wait(tl + C::TM_S, sr);
 
       float s[128];
 #pragma unroll
@@ -283,34 +269,21 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
         l *= alpha;
       }
       const float mc = (m_ref == -INFINITY) ? 0.f : m_ref * c2;
-      float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+      float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 128; c += 4) {
-        s[c] = ex2_approx(fmaf(s[c], c2, -mc));
-        s[c + 1] = ex2_approx(fmaf(s[c + 1], c2, -mc));
-        s[c + 2] = ex2_approx(fmaf(s[c + 2], c2, -mc));
-        s[c + 3] = ex2_approx(fmaf(s[c + 3], c2, -mc));
-        rs0 += s[c];
-        rs1 += s[c + 1];
-        rs2 += s[c + 2];
-        rs3 += s[c + 3];
-      }
-      l += (rs0 + rs1) + (rs2 + rs3);
-
-      // P and O may only change once PV_{j-1} has finished reading/writing them.
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, wait_bounded(o_done, (j - 1) & 1, abort_flag, p.ws, 10))) {
-          ok = false;
-          break;
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(fmaf(s[64 * half + 2 * i], c2, -mc));
+          const float p1 = ex2_approx(fmaf(s[64 * half + 2 * i + 1], c2, -mc));
+          rs0 += p0;
+          rs1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
         }
-        tc_fence_after();
+        tmem_st32(tl + C::TM_S + 32u * half, pk);  // P over the first 64 columns of S
       }
-#pragma unroll
-      for (int cc = 0; cc < 16; ++cc) {
-        const uint32_t addr = sP + (cc >> 3) * C::BOX + row * 128 + ((((uint32_t)cc & 7u) ^ ((uint32_t)row & 7u)) << 4);
-        st_shared_v4(addr, pack_bf16x2(s[8 * cc + 0], s[8 * cc + 1]), pack_bf16x2(s[8 * cc + 2], s[8 * cc + 3]),
-                     pack_bf16x2(s[8 * cc + 4], s[8 * cc + 5]), pack_bf16x2(s[8 * cc + 6], s[8 * cc + 7]));
-      }
+      l += rs0 + rs1;
       if (__any_sync(0xffffffffu, scale_o)) {
         const float a = scale_o ? alpha : 1.f;
 #pragma unroll
@@ -321,15 +294,14 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
           tmem_st32(tl + C::TM_O + 32u * cb, o);
         }
-        tmem_st_wait();
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
     }
 
     if (ok && n_kv > 0) {
-      ok = __all_sync(0xffffffffu, wait_bounded(o_done, (n_kv - 1) & 1, abort_flag, p.ws, 11));
+      ok = __all_sync(0xffffffffu, wait_bounded(o_done, 0, abort_flag, p.ws, 11));
       if (ok) tc_fence_after();
     }
     if (ok) {
@@ -375,8 +347,8 @@ __global__ void __launch_bounds__(192, 1) attn_fwd_tc_kernel(const __grid_consta
     // Let copies and MMAs already in flight land before the block exits.
     if (warp == 0 && lane == 0) {
       if (issued[2]) drain_wait(q_full, 0);
-      for (int j = max(0, issued[0] - NS); j < issued[0]; ++j) drain_wait(k_full + (j % NS), (j / NS) & 1);
-      for (int j = max(0, issued[1] - NS); j < issued[1]; ++j) drain_wait(v_full + (j % NS), (j / NS) & 1);
+      if (issued[0]) drain_wait(k_full, (issued[0] - 1) & 1);
+      if (issued[1]) drain_wait(v_full, (issued[1] - 1) & 1);
     }
     if (warp == 1 && lane == 0 && n_kv > 0) {
       umma_commit(drain);
@@ -453,6 +425,7 @@ cudaError_t launch_attn_bf16_tc(const AttnArgs& a, std::string* err) {
   p.out_map = a.out_map;
   p.ws = a.ws;
   p.lse_ld = a.lse_ld;
+  p.n_tiles = a.n_tiles;
   p.H = a.H;
   p.Hkv = a.Hkv;
   p.scale = a.scale;
