@@ -18,7 +18,7 @@ from typing import Optional, Sequence
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "lib", "libcpattn.so")
+LIB_PATH = os.environ.get("CPATTN_LIB") or os.path.join(_PKG, "lib", "libcpattn.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "cpattn.h")
 
 OK, INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA_ERROR, DEVICE_FAULT = range(6)
