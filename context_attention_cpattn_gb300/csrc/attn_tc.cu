@@ -256,9 +256,16 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
       }
-      float mx = s[0];
+      // row max: four chains of three-input max
+      float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      for (int c = 0; c < 128; c += 8) {
+        m0 = fmax3(m0, s[c], s[c + 1]);
+        m1 = fmax3(m1, s[c + 2], s[c + 3]);
+        m2 = fmax3(m2, s[c + 4], s[c + 5]);
+        m3 = fmax3(m3, s[c + 6], s[c + 7]);
+      }
+      const float mx = fmax3(m0, m1, fmaxf(m2, m3));
 
       float alpha = 1.f;
       bool scale_o = false;
@@ -269,21 +276,25 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
         l *= alpha;
       }
       const float mc = (m_ref == -INFINITY) ? 0.f : m_ref * c2;
-      float rs0 = 0.f, rs1 = 0.f;
+      // exponents two at a time on the packed FP32 pipe: x = s*c2 - mc
+      const float2 c2v = make_float2(c2, c2), nmc = make_float2(-mc, -mc);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2_approx(fmaf(s[64 * half + 2 * i], c2, -mc));
-          const float p1 = ex2_approx(fmaf(s[64 * half + 2 * i + 1], c2, -mc));
-          rs0 += p0;
-          rs1 += p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), c2v, nmc);
+          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          if (i & 1)
+            acc1 = __fadd2_rn(acc1, e);
+          else
+            acc0 = __fadd2_rn(acc0, e);
+          pk[i] = pack_bf16x2(e.x, e.y);
         }
         tmem_st32(tl + C::TM_S + 32u * half, pk);  // P over the first 64 columns of S
       }
-      l += rs0 + rs1;
+      l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       if (__any_sync(0xffffffffu, scale_o)) {
         const float a = scale_o ? alpha : 1.f;
 #pragma unroll
