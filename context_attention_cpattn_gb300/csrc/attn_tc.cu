@@ -43,6 +43,7 @@
 // stream stay in L2.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -80,7 +81,7 @@ struct TcCfg {
   static constexpr uint32_t OFF_K = Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_V + KV_BYTES;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 128;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // 19 mbarriers (152 bytes) fit below
   static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 256;              // S (P aliased) | O
   static constexpr uint32_t TM_S = 0, TM_O = 128;
@@ -98,6 +99,21 @@ struct KvCursor {
   }
 };
 
+// Work item i -> (KV head g, query tile, query head inside the group): the
+// items of one KV head are consecutive, query tiles longest-first.
+struct Item {
+  int tile_id, h, g;
+};
+__device__ __forceinline__ Item item_of(int i, int n_tiles, int G) {
+  Item it;
+  const int hq = i % G;
+  const int rest = i / G;
+  it.tile_id = rest % n_tiles;
+  it.g = rest / n_tiles;
+  it.h = it.g * G + hq;
+  return it;
+}
+
 template <int D, bool kPartial>
 __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<D>;
@@ -109,31 +125,30 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = bars + 2;
-  uint64_t* v_full = bars + 3;
-  uint64_t* v_empty = bars + 4;
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* o_done = bars + 7;
-  uint64_t* drain = bars + 8;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = bars + 3;
+  uint64_t* v_full = bars + 4;
+  uint64_t* v_empty = bars + 5;
+  uint64_t* s_full = bars + 6;
+  uint64_t* p_full = bars + 7;
+  uint64_t* o_done = bars + 8;
+  uint64_t* o_free = bars + 9;
+  uint64_t* drain = bars + 10;
+  uint64_t* item_full = bars + 11;   // [4] ring of work items handed from the producer
+  uint64_t* item_empty = bars + 15;  // [4]
+  int* item_ring = reinterpret_cast<int*>(smem + C::OFF_MISC + 32);  // [4]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
-  int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);  // [0] K loads, [1] V loads, [2] Q
+  int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);  // loads issued: [0] K, [1] V, [2] Q
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // block -> (KV head g, query tile, query head inside the group)
   const int G = p.H / p.Hkv;
-  const int hq = blockIdx.x % G;
-  const int rest = blockIdx.x / G;
-  const int tile_id = rest % p.n_tiles;
-  const int g = rest / p.n_tiles;
-  const int h = g * G + hq;
-  const QTile tile = p.tiles[tile_id];
-  const int n_kv = tile.n_kv_tiles;
+  const int n_items = p.n_tiles * p.H;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     mbar_init(k_full, 1);
     mbar_init(k_empty, 1);
     mbar_init(v_full, 1);
@@ -141,7 +156,12 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
     mbar_init(s_full, 1);
     mbar_init(p_full, 128);
     mbar_init(o_done, 1);
+    mbar_init(o_free, 128);
     mbar_init(drain, 1);
+    for (int r = 0; r < 4; ++r) {
+      mbar_init(item_full + r, 1);
+      mbar_init(item_empty + r, 129);  // the MMA thread and the 128 softmax threads
+    }
     *abort_flag = 0;
     issued[0] = issued[1] = issued[2] = 0;
     fence_mbarrier_init();
@@ -156,35 +176,61 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // The producer hands out work items: the block's first item is blockIdx.x,
+  // later ones come from an atomic counter (dynamic, longest-first order), and
+  // each is passed to the MMA and softmax warps through a 4-deep ring.  Every
+  // role counts KV tiles and items across items, so the single-buffer barriers
+  // keep alternating phases from one item to the next.
+  auto take_item = [&](int k, uint32_t where) -> int {  // consumers: item k of this block, or -1
+    if (!wait_bounded(item_full + (k & 3), (k >> 2) & 1, abort_flag, p.ws, where)) return -2;
+    const int i = item_ring[k & 3];
+    mbar_arrive(item_empty + (k & 3));
+    return i;
+  };
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_kv > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-      for (int kb = 0; kb < C::KB; ++kb)
-        tma_load_3d(smem + kb * C::BOX, &p.tm_q, q_full, kb * 64, h, tile.q_row0);
-      issued[2] = 1;
-      KvCursor c{tile.run_begin, 0};
-      for (int j = 0; j < n_kv; ++j) {
-        const int row = p.runs[c.r].kv_row0 + c.off;
-        if (j > 0 && !wait_bounded(k_empty, (j - 1) & 1, abort_flag, p.ws, 1)) break;
-        mbar_arrive_expect_tx(k_full, C::KV_BYTES);
+      int kc = 0, qc = 0;
+      bool ok = true;
+      int i = blockIdx.x;
+      for (int k = 0; ok; ++k) {
+        if (k >= 4 && !wait_bounded(item_empty + (k & 3), ((k >> 2) - 1) & 1, abort_flag, p.ws, 14)) break;
+        item_ring[k & 3] = (i < n_items) ? i : -1;
+        mbar_arrive(item_full + (k & 3));
+        if (i >= n_items) break;
+        const Item it = item_of(i, p.n_tiles, G);
+        const int n_kv = p.tiles[it.tile_id].n_kv_tiles;
+        i = (int)gridDim.x + (int)atomicAdd(&p.ws->next_item, 1u);
+        if (n_kv == 0) continue;
+        // Q of this item once every S MMA of the previous item has read its Q
+        if (qc > 0 && !wait_bounded(q_empty, (qc - 1) & 1, abort_flag, p.ws, 1)) break;
+        mbar_arrive_expect_tx(q_full, C::Q_BYTES);
         for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(smem + C::OFF_K + kb * C::BOX, &p.tm_k, k_full, kb * 64, g, row);
-        issued[0] = j + 1;
-        if (j > 0 && !wait_bounded(v_empty, (j - 1) & 1, abort_flag, p.ws, 2)) break;
-        mbar_arrive_expect_tx(v_full, C::KV_BYTES);
-        for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(smem + C::OFF_V + kb * C::BOX, &p.tm_v, v_full, kb * 64, g, row);
-        issued[1] = j + 1;
-        c.next(p.runs);
+          tma_load_3d(smem + kb * C::BOX, &p.tm_q, q_full, kb * 64, it.h, p.tiles[it.tile_id].q_row0);
+        issued[2] = ++qc;
+        KvCursor c{p.tiles[it.tile_id].run_begin, 0};
+        for (int j = 0; j < n_kv; ++j, ++kc) {
+          const int row = p.runs[c.r].kv_row0 + c.off;
+          if (kc > 0 && !wait_bounded(k_empty, (kc - 1) & 1, abort_flag, p.ws, 2)) { ok = false; break; }
+          mbar_arrive_expect_tx(k_full, C::KV_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(smem + C::OFF_K + kb * C::BOX, &p.tm_k, k_full, kb * 64, it.g, row);
+          issued[0] = kc + 1;
+          if (kc > 0 && !wait_bounded(v_empty, (kc - 1) & 1, abort_flag, p.ws, 3)) { ok = false; break; }
+          mbar_arrive_expect_tx(v_full, C::KV_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(smem + C::OFF_V + kb * C::BOX, &p.tm_v, v_full, kb * 64, it.g, row);
+          issued[1] = kc + 1;
+          c.next(p.runs);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_kv > 0) {
+    if (lane == 0) {
       const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       auto issue_s = [&]() {
 #pragma unroll
@@ -194,128 +240,154 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
                        IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
-      bool ok = wait_bounded(q_full, 0, abort_flag, p.ws, 3) && wait_bounded(k_full, 0, abort_flag, p.ws, 4);
-      if (ok) {
+      int kc = 0, qc = 0, oc = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int i = take_item(k, 15);
+        if (i < 0) break;
+        const int n_kv = p.tiles[item_of(i, p.n_tiles, G).tile_id].n_kv_tiles;
+        if (n_kv == 0) continue;
+        ok = wait_bounded(q_full, qc & 1, abort_flag, p.ws, 4) && wait_bounded(k_full, kc & 1, abort_flag, p.ws, 5);
+        if (!ok) break;
+        ++qc;
         tc_fence_after();
         issue_s();
-        if (n_kv > 1) umma_commit(k_empty);
+        umma_commit(k_empty);
+        if (n_kv == 1) umma_commit(q_empty);
         umma_commit(s_full);
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        ok = wait_bounded(p_full, j & 1, abort_flag, p.ws, 5) && wait_bounded(v_full, j & 1, abort_flag, p.ws, 6);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA: P columns 8kk.., V rows 16kk..
-          umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 8 * kk, smem_desc_sw128(sV + kk * 2048, C::BOX, 1024),
-                       IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-        if (j + 1 < n_kv) {
-          umma_commit(v_empty);
-          ok = wait_bounded(k_full, (j + 1) & 1, abort_flag, p.ws, 7);
+        for (int j = 0; j < n_kv; ++j, ++kc) {
+          ok = wait_bounded(p_full, kc & 1, abort_flag, p.ws, 6) && wait_bounded(v_full, kc & 1, abort_flag, p.ws, 7);
+          // the first PV of an item overwrites O: the previous item's epilogue must have read it
+          if (ok && j == 0 && oc > 0) ok = wait_bounded(o_free, (oc - 1) & 1, abort_flag, p.ws, 8);
           if (!ok) break;
           tc_fence_after();
-          issue_s();
-          if (j + 2 < n_kv) umma_commit(k_empty);
-          umma_commit(s_full);
-        } else {
-          umma_commit(o_done);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA: P columns 8kk.., V rows 16kk..
+            umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 8 * kk, smem_desc_sw128(sV + kk * 2048, C::BOX, 1024),
+                         IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(v_empty);
+          if (j + 1 < n_kv) {
+            ok = wait_bounded(k_full, (kc + 1) & 1, abort_flag, p.ws, 9);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s();
+            umma_commit(k_empty);
+            if (j + 2 == n_kv) umma_commit(q_empty);
+            umma_commit(s_full);
+          } else {
+            umma_commit(o_done);
+          }
         }
+        ++oc;
       }
+      // every commit above has landed before the block can exit
+      umma_commit(drain);
+      drain_wait(drain, 0);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-    const int q_pos = tile.q_pos0 + row;
     const float c2 = p.scale_log2;
-    float m_ref = -INFINITY, l = 0.f;
+    int kc = 0, oc = 0;
     bool ok = true;
-    KvCursor cur{tile.run_begin, 0};
-    for (int j = 0; j < n_kv; ++j) {
-      const KvRun run = p.runs[cur.r];
-      const int n_keys = min(128, run.kv_len - cur.off);
-      const int kpos0 = run.kv_pos0 + cur.off;
-      const bool tile_mask = (n_keys < 128) || (run.causal && kpos0 + n_keys - 1 > tile.q_pos0);
-      cur.next(p.runs);
+    for (int k = 0; ok; ++k) {
+      const int i = take_item(k, 16);
+      if (!__all_sync(0xffffffffu, i != -2)) break;
+      if (i < 0) break;
+      const int tile_id = item_of(i, p.n_tiles, G).tile_id;
+      const int n_kv = p.tiles[tile_id].n_kv_tiles;
+      const int q_pos0 = p.tiles[tile_id].q_pos0;
+      float m_ref = -INFINITY, l = 0.f;
+      KvCursor cur{p.tiles[tile_id].run_begin, 0};
+      for (int j = 0; j < n_kv; ++j, ++kc) {
+        const KvRun run = p.runs[cur.r];
+        const int n_keys = min(128, run.kv_len - cur.off);
+        const int kpos0 = run.kv_pos0 + cur.off;
+        const bool tile_mask = (n_keys < 128) || (run.causal && kpos0 + n_keys - 1 > q_pos0);
+        cur.next(p.runs);
 
-      if (!__all_sync(0xffffffffu, wait_bounded(s_full, j & 1, abort_flag, p.ws, 9))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld128_wait(tl + C::TM_S, sr);
-
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-      if (tile_mask) {
-        int lim = n_keys;
-        if (run.causal) lim = min(lim, q_pos - kpos0 + 1);
-#pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
-      }
-      // row max: four chains of three-input max
-      float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-        m0 = fmax3(m0, s[c], s[c + 1]);
-        m1 = fmax3(m1, s[c + 2], s[c + 3]);
-        m2 = fmax3(m2, s[c + 4], s[c + 5]);
-        m3 = fmax3(m3, s[c + 6], s[c + 7]);
-      }
-      const float mx = fmax3(m0, m1, fmaxf(m2, m3));
-
-      float alpha = 1.f;
-      bool scale_o = false;
-      if (mx > m_ref + p.thresh_raw) {
-        alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx((m_ref - mx) * c2);
-        scale_o = (j > 0) && (m_ref != -INFINITY);
-        m_ref = mx;
-        l *= alpha;
-      }
-      const float mc = (m_ref == -INFINITY) ? 0.f : m_ref * c2;
-      // exponents two at a time on the packed FP32 pipe: x = s*c2 - mc
-      const float2 c2v = make_float2(c2, c2), nmc = make_float2(-mc, -mc);
-      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 x = __ffma2_rn(make_float2(s[64 * half + 2 * i], s[64 * half + 2 * i + 1]), c2v, nmc);
-          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          if (i & 1)
-            acc1 = __fadd2_rn(acc1, e);
-          else
-            acc0 = __fadd2_rn(acc0, e);
-          pk[i] = pack_bf16x2(e.x, e.y);
+        if (!__all_sync(0xffffffffu, wait_bounded(s_full, kc & 1, abort_flag, p.ws, 10))) {
+          ok = false;
+          break;
         }
-        tmem_st32(tl + C::TM_S + 32u * half, pk);  // P over the first 64 columns of S
-      }
-      l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
-      if (__any_sync(0xffffffffu, scale_o)) {
-        const float a = scale_o ? alpha : 1.f;
-#pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t o[32];
-          tmem_ld32_wait(tl + C::TM_O + 32u * cb, o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-          tmem_st32(tl + C::TM_O + 32u * cb, o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
+        tc_fence_after();
+        uint32_t sr[128];
+        tmem_ld128_wait(tl + C::TM_S, sr);
 
-    if (ok && n_kv > 0) {
-      ok = __all_sync(0xffffffffu, wait_bounded(o_done, 0, abort_flag, p.ws, 11));
-      if (ok) tc_fence_after();
-    }
-    if (ok) {
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        if (tile_mask) {
+          int lim = n_keys;
+          if (run.causal) lim = min(lim, q_pos0 + row - kpos0 + 1);
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+        }
+        // row max: four chains of three-input max
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+          m0 = fmax3(m0, s[c], s[c + 1]);
+          m1 = fmax3(m1, s[c + 2], s[c + 3]);
+          m2 = fmax3(m2, s[c + 4], s[c + 5]);
+          m3 = fmax3(m3, s[c + 6], s[c + 7]);
+        }
+        const float mx = fmax3(m0, m1, fmaxf(m2, m3));
+
+        float alpha = 1.f;
+        bool scale_o = false;
+        if (mx > m_ref + p.thresh_raw) {
+          alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx((m_ref - mx) * c2);
+          scale_o = (j > 0) && (m_ref != -INFINITY);
+          m_ref = mx;
+          l *= alpha;
+        }
+        const float mc = (m_ref == -INFINITY) ? 0.f : m_ref * c2;
+        // exponents two at a time on the packed FP32 pipe: x = s*c2 - mc
+        const float2 c2v = make_float2(c2, c2), nmc = make_float2(-mc, -mc);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const float2 x = __ffma2_rn(make_float2(s[64 * half + 2 * q], s[64 * half + 2 * q + 1]), c2v, nmc);
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            if (q & 1)
+              acc1 = __fadd2_rn(acc1, e);
+            else
+              acc0 = __fadd2_rn(acc0, e);
+            pk[q] = pack_bf16x2(e.x, e.y);
+          }
+          tmem_st32(tl + C::TM_S + 32u * half, pk);  // P over the first 64 columns of S
+        }
+        l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        if (__any_sync(0xffffffffu, scale_o)) {
+          const float a = scale_o ? alpha : 1.f;
+#pragma unroll
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t o[32];
+            tmem_ld32_wait(tl + C::TM_O + 32u * cb, o);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * a);
+            tmem_st32(tl + C::TM_O + 32u * cb, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full);
+      }
+      if (!ok) break;
+
+      if (n_kv > 0) {
+        if (!__all_sync(0xffffffffu, wait_bounded(o_done, oc & 1, abort_flag, p.ws, 11))) break;
+        tc_fence_after();
+      }
+      // epilogue: O / l and LSE at the output rows
+      const Item it = item_of(i, p.n_tiles, G);
+      const QTile tile = p.tiles[it.tile_id];
       const bool valid_row = row < tile.q_rows;
       const bool has = l > 0.f;
       const float inv_l = has ? 1.f / l : 0.f;
@@ -328,26 +400,33 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
           tmem_ld32_wait(tl + C::TM_O + 32u * cb, o);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = 0u;
+          for (int q = 0; q < 32; ++q) o[q] = 0u;
         }
         if (valid_row) {
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = has ? __uint_as_float(o[i]) * inv_l : 0.f;
+          for (int q = 0; q < 32; ++q) v[q] = has ? __uint_as_float(o[q]) * inv_l : 0.f;
           if (kPartial) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + (out_row * p.H + h) * D + 32 * cb);
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + (out_row * p.H + it.h) * D + 32 * cb);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (out_row * p.H + h) * D + 32 * cb);
+            uint4* dst =
+                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (out_row * p.H + it.h) * D + 32 * cb);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                  pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
           }
         }
       }
-      if (valid_row) p.lse[(int64_t)h * p.lse_ld + out_row] = has ? m_ref * p.scale + logf(l) : -INFINITY;
+      if (valid_row) p.lse[(int64_t)it.h * p.lse_ld + out_row] = has ? m_ref * p.scale + logf(l) : -INFINITY;
+      if (n_kv > 0) {
+        // O has been read: the next item's first PV may overwrite it
+        tc_fence_before();
+        mbar_arrive(o_free);
+        ++oc;
+      }
     }
   }
 
@@ -357,13 +436,9 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
   if (*abort_flag) {
     // Let copies and MMAs already in flight land before the block exits.
     if (warp == 0 && lane == 0) {
-      if (issued[2]) drain_wait(q_full, 0);
+      if (issued[2]) drain_wait(q_full, (issued[2] - 1) & 1);
       if (issued[0]) drain_wait(k_full, (issued[0] - 1) & 1);
       if (issued[1]) drain_wait(v_full, (issued[1] - 1) & 1);
-    }
-    if (warp == 1 && lane == 0 && n_kv > 0) {
-      umma_commit(drain);
-      drain_wait(drain, 0);
     }
     __syncthreads();
   }
@@ -442,12 +517,14 @@ cudaError_t launch_attn_bf16_tc(const AttnArgs& a, std::string* err) {
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.thresh_raw = 8.0f / p.scale_log2;
-  const int64_t blocks = (int64_t)a.n_tiles * a.H;
-  if (blocks == 0) return cudaSuccess;
-  if (blocks > 0x7fffffff) {
+  const int64_t items = (int64_t)a.n_tiles * a.H;
+  if (items == 0) return cudaSuccess;
+  if (items > 0x7fffffff) {
     *err = "too many query tiles";
     return cudaErrorInvalidValue;
   }
+  // persistent blocks, two per SM, each walking items blockIdx.x, +gridDim.x, ...
+  const int64_t blocks = std::min<int64_t>(items, 2 * (int64_t)num_sms());
   if (a.D == 128) return a.partial ? launch_tc<128, true>(p, (int)blocks, a.stream)
                                    : launch_tc<128, false>(p, (int)blocks, a.stream);
   return a.partial ? launch_tc<64, true>(p, (int)blocks, a.stream) : launch_tc<64, false>(p, (int)blocks, a.stream);

@@ -37,7 +37,8 @@ typedef struct WsHeader {
   uint32_t fault;     // 0 = none; else a CPATTN_FAULT_* code
   uint32_t info;      // where (block index)
   uint32_t detail;    // which wait / value
-  uint32_t pad[61];
+  uint32_t next_item; // work counter of persistent kernels (items handed out beyond the first wave)
+  uint32_t pad[60];
 } WsHeader;
 
 #ifdef __cplusplus
