@@ -72,13 +72,15 @@ cpattn_status_t check_shape(int H, int Hkv, int D, cpattn_dtype_t dt) {
   return CPATTN_OK;
 }
 
-void tile_sizes(cpattn_dtype_t dt, int* tm, int* tn) {
+void tile_sizes(cpattn_dtype_t dt, int* tm, int* tn, bool* pair) {
   if (dt == CPATTN_DTYPE_BF16) {
     *tm = cpattn::kTcTileM;
     *tn = cpattn::kTcTileN;
+    *pair = cpattn::kTcPair;
   } else {
     *tm = cpattn::kSimtTileM;
     *tn = cpattn::kSimtTileN;
+    *pair = cpattn::kSimtPair;
   }
 }
 
@@ -295,8 +297,9 @@ cpattn_status_t cpattn_workspace_size(const cpattn_plan_t* plan, int32_t H, int3
   if (causal && plan->mode == CPATTN_MODE_GRID2D)
     return fail(CPATTN_UNSUPPORTED, "causal masks are not defined for grid2d plans");
   int tm, tn;
-  tile_sizes(dtype, &tm, &tn);
-  auto wl = cpattn::get_worklist(*const_cast<cpattn_plan_t*>(plan), causal != 0, tm, tn, -1, 0);
+  bool pair;
+  tile_sizes(dtype, &tm, &tn, &pair);
+  auto wl = cpattn::get_worklist(*const_cast<cpattn_plan_t*>(plan), causal != 0, tm, tn, pair, -1, 0);
   *bytes = ws_layout(*plan, *wl, H, Hkv, D, elem_size(dtype)).total;
   return CPATTN_OK;
 }
@@ -313,14 +316,15 @@ static cpattn_status_t run_attention(const cpattn_plan_t* cplan, const void* q, 
   cpattn_plan_t* plan = const_cast<cpattn_plan_t*>(cplan);
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int tm, tn;
-  tile_sizes(dtype, &tm, &tn);
+  bool pair;
+  tile_sizes(dtype, &tm, &tn, &pair);
   // the workspace must hold the whole-forward layout (an upper bound for one step)
-  auto wl_all = cpattn::get_worklist(*plan, causal != 0, tm, tn, -1, 0);
+  auto wl_all = cpattn::get_worklist(*plan, causal != 0, tm, tn, pair, -1, 0);
   const size_t es = elem_size(dtype);
   const WsLayout L_all = ws_layout(*plan, *wl_all, H, Hkv, D, es);
   if (ws_bytes < L_all.total)
     return fail(CPATTN_WORKSPACE, "workspace too small: need " + std::to_string(L_all.total) + " bytes");
-  auto wl = (q_rank < 0) ? wl_all : cpattn::get_worklist(*plan, causal != 0, tm, tn, q_rank, step);
+  auto wl = (q_rank < 0) ? wl_all : cpattn::get_worklist(*plan, causal != 0, tm, tn, pair, q_rank, step);
   WsLayout L = ws_layout(*plan, *wl, H, Hkv, D, es);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   s = upload_worklist(plan, *wl, L, ws, stream);

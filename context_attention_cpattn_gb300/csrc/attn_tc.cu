@@ -87,15 +87,28 @@ struct TcCfg {
   static constexpr uint32_t TM_S = 0, TM_O = 128;
 };
 
-// Advances through the KV runs of a q tile in 128-key steps.
-struct KvCursor {
-  int r, off;
-  __device__ void next(const KvRun* runs) {
-    off += 128;
-    if (off >= runs[r].kv_len) {
+// Walks the KV runs of a q tile in pieces of up to 64 keys; a KV tile of the
+// kernel is two consecutive pieces (keys 0-63 and 64-127 of the tile), which
+// may come from different runs.  After the last run it yields empty pieces.
+struct Piece {
+  int row0, pos0, len, causal;
+};
+struct PieceCursor {
+  int r, off, r_end;
+  __device__ Piece next(const KvRun* runs) {
+    Piece pc{0, 0, 0, 0};
+    if (r >= r_end) return pc;
+    const KvRun run = runs[r];
+    pc.row0 = run.kv_row0 + off;
+    pc.pos0 = run.kv_pos0 + off;
+    pc.len = min(64, run.kv_len - off);
+    pc.causal = run.causal;
+    off += 64;
+    if (off >= run.kv_len) {
       ++r;
       off = 0;
     }
+    return pc;
   }
 };
 
@@ -211,20 +224,26 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
         for (int kb = 0; kb < C::KB; ++kb)
           tma_load_3d(smem + kb * C::BOX, &p.tm_q, q_full, kb * 64, it.h, p.tiles[it.tile_id].q_row0);
         issued[2] = ++qc;
-        KvCursor c{p.tiles[it.tile_id].run_begin, 0};
+        PieceCursor c{p.tiles[it.tile_id].run_begin, 0, p.tiles[it.tile_id].run_end};
         for (int j = 0; j < n_kv; ++j, ++kc) {
-          const int row = p.runs[c.r].kv_row0 + c.off;
+          const Piece pa = c.next(p.runs);
+          const Piece pb = c.next(p.runs);
+          // an empty second piece reloads the first (finite values, masked out)
+          const int row_a = pa.row0, row_b = pb.len > 0 ? pb.row0 : pa.row0;
           if (kc > 0 && !wait_bounded(k_empty, (kc - 1) & 1, abort_flag, p.ws, 2)) { ok = false; break; }
           mbar_arrive_expect_tx(k_full, C::KV_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(smem + C::OFF_K + kb * C::BOX, &p.tm_k, k_full, kb * 64, it.g, row);
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(smem + C::OFF_K + kb * C::BOX, &p.tm_k, k_full, kb * 64, it.g, row_a);
+            tma_load_3d(smem + C::OFF_K + kb * C::BOX + C::BOX / 2, &p.tm_k, k_full, kb * 64, it.g, row_b);
+          }
           issued[0] = kc + 1;
           if (kc > 0 && !wait_bounded(v_empty, (kc - 1) & 1, abort_flag, p.ws, 3)) { ok = false; break; }
           mbar_arrive_expect_tx(v_full, C::KV_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb)
-            tma_load_3d(smem + C::OFF_V + kb * C::BOX, &p.tm_v, v_full, kb * 64, it.g, row);
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(smem + C::OFF_V + kb * C::BOX, &p.tm_v, v_full, kb * 64, it.g, row_a);
+            tma_load_3d(smem + C::OFF_V + kb * C::BOX + C::BOX / 2, &p.tm_v, v_full, kb * 64, it.g, row_b);
+          }
           issued[1] = kc + 1;
-          c.next(p.runs);
         }
       }
     }
@@ -300,13 +319,12 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
       const int n_kv = p.tiles[tile_id].n_kv_tiles;
       const int q_pos0 = p.tiles[tile_id].q_pos0;
       float m_ref = -INFINITY, l = 0.f;
-      KvCursor cur{p.tiles[tile_id].run_begin, 0};
+      PieceCursor cur{p.tiles[tile_id].run_begin, 0, p.tiles[tile_id].run_end};
       for (int j = 0; j < n_kv; ++j, ++kc) {
-        const KvRun run = p.runs[cur.r];
-        const int n_keys = min(128, run.kv_len - cur.off);
-        const int kpos0 = run.kv_pos0 + cur.off;
-        const bool tile_mask = (n_keys < 128) || (run.causal && kpos0 + n_keys - 1 > q_pos0);
-        cur.next(p.runs);
+        const Piece pa = cur.next(p.runs);
+        const Piece pb = cur.next(p.runs);
+        const bool tile_mask = (pa.len < 64) || (pb.len < 64) || (pa.causal && pa.pos0 + 63 > q_pos0) ||
+                               (pb.causal && pb.pos0 + 63 > q_pos0);
 
         if (!__all_sync(0xffffffffu, wait_bounded(s_full, kc & 1, abort_flag, p.ws, 10))) {
           ok = false;
@@ -320,10 +338,14 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
         if (tile_mask) {
-          int lim = n_keys;
-          if (run.causal) lim = min(lim, q_pos0 + row - kpos0 + 1);
+          // keys 0-63 come from piece a, 64-127 from piece b: each is a prefix mask
+          int lim_a = pa.len, lim_b = pb.len;
+          if (pa.causal) lim_a = min(lim_a, q_pos0 + row - pa.pos0 + 1);
+          if (pb.causal) lim_b = min(lim_b, q_pos0 + row - pb.pos0 + 1);
 #pragma unroll
-          for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
+          for (int c = 0; c < 64; ++c) s[c] = (c < lim_a) ? s[c] : -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[64 + c] = (c < lim_b) ? s[64 + c] : -INFINITY;
         }
         // row max: four chains of three-input max
         float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
@@ -466,8 +488,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // [rows, heads, D] bf16 viewed as a 3-D tensor (D, heads, rows); box = 64
-// columns x 1 head x 128 rows, 128-byte swizzle.
-static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, std::string* err) {
+// columns x 1 head x box_rows rows (128 for Q, 64 for a K/V piece), 128-byte
+// swizzle.
+static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
+                     std::string* err) {
   auto enc = tensor_map_encoder();
   if (!enc) {
     *err = "cuTensorMapEncodeTiled is not available from the driver";
@@ -475,7 +499,7 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, 
   }
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -500,9 +524,9 @@ static cudaError_t launch_tc(const TcParams& p, int n_blocks, cudaStream_t strea
 cudaError_t launch_attn_bf16_tc(const AttnArgs& a, std::string* err) {
   TcParams p;
   memset(&p, 0, sizeof(p));
-  if (!make_map(&p.tm_q, a.q, a.q_rows_total, a.H, a.D, err) ||
-      !make_map(&p.tm_k, a.k, a.kv_rows_total, a.Hkv, a.D, err) ||
-      !make_map(&p.tm_v, a.v, a.kv_rows_total, a.Hkv, a.D, err))
+  if (!make_map(&p.tm_q, a.q, a.q_rows_total, a.H, a.D, 128, err) ||
+      !make_map(&p.tm_k, a.k, a.kv_rows_total, a.Hkv, a.D, 64, err) ||
+      !make_map(&p.tm_v, a.v, a.kv_rows_total, a.Hkv, a.D, 64, err))
     return cudaErrorInvalidValue;
   p.tiles = a.tiles;
   p.runs = a.runs;

@@ -32,9 +32,13 @@ struct AttnArgs {
   cudaStream_t stream = nullptr;
 };
 
-// q tile / kv tile sizes each attention kernel was built for
-constexpr int kTcTileM = 128, kTcTileN = 128;
+// q tile / kv piece sizes each attention kernel was built for.  The tensor-core
+// kernel's 128-key tile is two 64-key pieces, which may come from different
+// runs (short chunks share a tile).
+constexpr int kTcTileM = 128, kTcTileN = 64;
+constexpr bool kTcPair = true;
 constexpr int kSimtTileM = 64, kSimtTileN = 32;
+constexpr bool kSimtPair = false;
 
 cudaError_t launch_attn_bf16_tc(const AttnArgs& a, std::string* err);
 cudaError_t launch_attn_fp32_simt(const AttnArgs& a, std::string* err);

@@ -183,7 +183,7 @@ static std::pair<size_t, size_t> seq_range(const std::vector<Segment>& segs, int
 }
 
 static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool causal, int tile_m,
-                                                int tile_n, int q_rank, int step) {
+                                                int tile_n, bool pair, int q_rank, int step) {
   auto wl = std::make_shared<WorkList>();
   const int cp = p.cp;
   const bool gathered = (p.mode == CPATTN_MODE_GRID2D);
@@ -241,6 +241,7 @@ static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool cau
           }
         }
         t.run_end = (int32_t)wl->runs.size();
+        if (pair) ntiles = (ntiles + 1) / 2;  // two pieces per kernel tile
         t.n_kv_tiles = (int32_t)ntiles;
         wl->total_kv_tiles += ntiles;
         wl->tiles.push_back(t);
@@ -255,13 +256,13 @@ static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool cau
   return wl;
 }
 
-std::shared_ptr<const WorkList> get_worklist(cpattn_plan_t& p, bool causal, int tile_m, int tile_n,
+std::shared_ptr<const WorkList> get_worklist(cpattn_plan_t& p, bool causal, int tile_m, int tile_n, bool pair,
                                              int q_rank, int step) {
-  WorkKey key{causal ? 1 : 0, tile_m, tile_n, q_rank, step};
+  WorkKey key{causal ? 1 : 0, tile_m, tile_n, pair ? 1 : 0, q_rank, step};
   std::lock_guard<std::mutex> lock(p.mu);
   auto it = p.cache.find(key);
   if (it != p.cache.end()) return it->second;
-  auto wl = build_worklist(p, causal, tile_m, tile_n, q_rank, step);
+  auto wl = build_worklist(p, causal, tile_m, tile_n, pair, q_rank, step);
   p.cache[key] = wl;
   return wl;
 }

@@ -29,10 +29,10 @@ struct WorkList {
 };
 
 struct WorkKey {
-  int causal, tile_m, tile_n, q_rank, step;  // q_rank = -1: every rank, every step
+  int causal, tile_m, tile_n, pair, q_rank, step;  // q_rank = -1: every rank, every step
   bool operator<(const WorkKey& o) const {
-    return std::tie(causal, tile_m, tile_n, q_rank, step) <
-           std::tie(o.causal, o.tile_m, o.tile_n, o.q_rank, o.step);
+    return std::tie(causal, tile_m, tile_n, pair, q_rank, step) <
+           std::tie(o.causal, o.tile_m, o.tile_n, o.pair, o.q_rank, o.step);
   }
 };
 
@@ -69,7 +69,9 @@ bool ring_entry(const cpattn_plan_t& p, int r, int t, bool causal, int32_t* kv_r
 
 // Work list of q tiles (tile_m rows) with their KV runs in ring order.
 // q_rank < 0: all ranks and all steps (whole forward); else one (rank, step).
-std::shared_ptr<const WorkList> get_worklist(cpattn_plan_t& p, bool causal, int tile_m, int tile_n,
+// Each run is cut into pieces of tile_n keys; with `pair`, two consecutive
+// pieces (possibly from different runs) form one KV tile of the kernel.
+std::shared_ptr<const WorkList> get_worklist(cpattn_plan_t& p, bool causal, int tile_m, int tile_n, bool pair,
                                              int q_rank, int step);
 
 }  // namespace cpattn

@@ -81,7 +81,8 @@ extern "C" cpattn_status_t cpattn_fwd_static(const cpattn_plan_t* cplan, const v
   cpattn_plan_t* plan = const_cast<cpattn_plan_t*>(cplan);
   const bool bf16 = dtype == CPATTN_DTYPE_BF16;
   const int tm = bf16 ? cpattn::kTcTileM : cpattn::kSimtTileM, tn = bf16 ? cpattn::kTcTileN : cpattn::kSimtTileN;
-  auto wl = cpattn::get_worklist(*plan, causal != 0, tm, tn, -1, 0);
+  const bool pair = bf16 ? cpattn::kTcPair : cpattn::kSimtPair;
+  auto wl = cpattn::get_worklist(*plan, causal != 0, tm, tn, pair, -1, 0);
   const size_t tb = wl->tiles.size() * sizeof(cpattn::QTile), rb = wl->runs.size() * sizeof(cpattn::KvRun);
   const size_t off_tiles = CPATTN_WS_HEADER_BYTES, off_runs = off_tiles + round256(tb);
   const size_t need = off_runs + round256(rb);
