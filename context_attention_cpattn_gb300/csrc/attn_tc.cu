@@ -1,46 +1,46 @@
 // bf16 packed varlen attention forward on the 5th-generation tensor cores
-// (tcgen05.mma, accumulators in TMEM, K/V/Q tiles staged by TMA).
+// (tcgen05.mma, accumulators in TMEM, Q/K/V tiles staged by TMA).
 //
-// One thread block computes one 128-row query tile of one head.  It walks the
-// tile's KV runs in ring order - at ring step t the queries of virtual rank r
-// see the KV shard of rank (r - t) mod cp ("Scaling video training with
-// parallelism", section 2, Ring Attention) - in 128-key tiles, and merges
-// every tile's partial into the running result by exact log-sum-exp
-// rescaling, so each ring step's partial (O_t, lse_t) is folded in as soon as
-// it is produced and never leaves the SM.
+// A work item is one 128-row query tile of one head.  It walks the tile's KV
+// runs in ring order - at ring step t the queries of virtual rank r see the
+// KV shard of rank (r - t) mod cp ("Scaling video training with parallelism",
+// section 2, Ring Attention) - in 64-key tiles, and merges every tile's
+// partial into the running result by exact log-sum-exp rescaling, so each
+// ring step's partial (O_t, lse_t) is folded in as soon as it is produced and
+// never leaves the SM.
 //
-// Two blocks share each SM (about 97 KB of shared memory and 256 TMEM
-// columns each), so one block's softmax, prologue and epilogue overlap the
-// other block's matrix multiplies.
+// Persistent blocks, two per SM (about 99 KB of shared memory and 256 TMEM
+// columns each).  The producer warp hands out work items (the first by block
+// index, the rest from an atomic counter, longest first) through a ring of
+// shared-memory slots.
 //
 // Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K_j and V_j into single buffers;
-//               K_{j+1} is loaded as soon as S_j = Q K_j^T has consumed K_j,
-//               V_{j+1} as soon as O += P_j V_j has consumed V_j.
-//   warp 1      TMEM allocator and MMA issuer (one thread), in order:
-//                 S_0, PV_0, S_1, PV_1, ...
-//                 S_j  = Q K_j^T  (M=128, N=128, K=D)   A, B from shared memory
-//                 O   += P_j V_j  (M=128, N=D,   K=128) A = P from TMEM, B = V
-//               P_j lives in TMEM over the columns of S_j; S_{j+1} is issued
-//               after PV_j, and tcgen05.mma ops from one thread run in issue
-//               order, so PV_j has read P_j before S_{j+1} overwrites it.
-//   warps 2-5   softmax + epilogue, one query row per thread: read S from
+//   warp 0      TMA producer: Q per item, then K_j and V_j through two-deep
+//               rings; K_j is refilled once S_j has read it, V_j once PV_j has.
+//   warp 1      TMEM allocator and MMA issuer (one thread).  TMEM holds two S
+//               buffers of 64 columns and O (128 columns).  Order per item:
+//                 S_0, S_1, PV_0, S_2, PV_1, S_3, ...
+//                 S_j  = Q K_j^T  (M=128, N=64, K=D)   A, B from shared memory
+//                 O   += P_j V_j  (M=128, N=D,  K=64)  A = P_j from TMEM, B = V_j
+//               so the scores of the next tile are computed while the softmax
+//               warps work on this one.  P_j is written over the first 32
+//               columns of S_j's buffer; S_{j+2} reuses that buffer after PV_j
+//               (tcgen05.mma ops from one thread run in issue order).
+//   warps 2-5   softmax + epilogue, one query row per thread: read S_j from
 //               TMEM, apply the causal / run-end mask from token positions,
 //               update the running max and sum, write P (bf16 pairs) back to
-//               TMEM, and rescale O in TMEM when the running max grows by more
-//               than 2^8 (otherwise the stale max is kept: O and the sum share
-//               it, so the final O/l is exact).  When S_j has landed, every
-//               earlier MMA - PV_{j-1} included - has finished, so O may be
-//               rescaled without a further wait.
+//               TMEM, and rescale O when the running max grows by more than
+//               2^8 (otherwise the stale max is kept: O and the sum share it,
+//               so the final O/l is exact).  A rescale first waits for PV_{j-1}.
 //
 // Shared-memory operand layouts (1024-byte aligned, SWIZZLE_128B):
-//   Q, K: [128 rows][64 columns] boxes, K-major (rows = M or N, columns = K).
-//   V:    [128 keys][64 d] boxes; as the B operand of P.V (N = d, K = keys)
-//         this is MN-major: 8-key groups 1024 B apart (SBO), 64-wide d
-//         blocks one box apart (LBO).
-// Dispatch order: blocks of one KV head (all its query heads, every query
-// tile longest-first) are consecutive, so the KV rows the resident blocks
-// stream stay in L2.
+//   Q:    [128 rows][64 columns] boxes, K-major.
+//   K_j:  [64 keys][64 columns] boxes, K-major (the B operand of S = Q K^T).
+//   V_j:  [64 keys][64 d] boxes; as the B operand of P.V (N = d, K = keys)
+//         this is MN-major: 8-key groups 1024 B apart (SBO), 64-wide d blocks
+//         one box apart (LBO).
+// Items of one KV head are consecutive (all its query heads, query tiles
+// longest-first), so the KV rows the resident blocks stream stay in L2.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -74,22 +74,21 @@ struct alignas(64) TcParams {
 
 template <int D>
 struct TcCfg {
-  static constexpr int KB = D / 64;                 // 64-column boxes per row
-  static constexpr uint32_t BOX = 128 * 128;        // 128 rows x 128 bytes
-  static constexpr uint32_t Q_BYTES = KB * BOX;
-  static constexpr uint32_t KV_BYTES = KB * BOX;
-  static constexpr uint32_t OFF_K = Q_BYTES;
-  static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + KV_BYTES;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // 19 mbarriers (152 bytes) fit below
+  static constexpr int KB = D / 64;                   // 64-column boxes per row
+  static constexpr uint32_t QBOX = 128 * 128;         // 128 rows x 128 bytes
+  static constexpr uint32_t KVBOX = 64 * 128;         // 64 rows x 128 bytes
+  static constexpr uint32_t Q_BYTES = KB * QBOX;
+  static constexpr uint32_t KV_BYTES = KB * KVBOX;    // one 64-key K or V tile
+  static constexpr uint32_t OFF_K = Q_BYTES;          // K[2]
+  static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;  // V[2]
+  static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // 26 mbarriers (208 bytes) fit below
   static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
-  static constexpr uint32_t TMEM_COLS = 256;              // S (P aliased) | O
-  static constexpr uint32_t TM_S = 0, TM_O = 128;
+  static constexpr uint32_t TMEM_COLS = 256;              // S0 | S1 | O
+  static constexpr uint32_t TM_S = 0, TM_O = 128;         // S buffer b at TM_S + 64 b
 };
 
-// Walks the KV runs of a q tile in pieces of up to 64 keys; a KV tile of the
-// kernel is two consecutive pieces (keys 0-63 and 64-127 of the tile), which
-// may come from different runs.  After the last run it yields empty pieces.
+// Walks the KV runs of a q tile in tiles of up to 64 keys.
 struct Piece {
   int row0, pos0, len, causal;
 };
@@ -130,7 +129,7 @@ __device__ __forceinline__ Item item_of(int i, int n_tiles, int G) {
 template <int D, bool kPartial>
 __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<D>;
-  constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, false, false);
+  constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
 
   extern __shared__ uint8_t smem_raw[];
@@ -139,21 +138,22 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* k_empty = bars + 3;
-  uint64_t* v_full = bars + 4;
-  uint64_t* v_empty = bars + 5;
-  uint64_t* s_full = bars + 6;
-  uint64_t* p_full = bars + 7;
-  uint64_t* o_done = bars + 8;
-  uint64_t* o_free = bars + 9;
-  uint64_t* drain = bars + 10;
-  uint64_t* item_full = bars + 11;   // [4] ring of work items handed from the producer
-  uint64_t* item_empty = bars + 15;  // [4]
-  int* item_ring = reinterpret_cast<int*>(smem + C::OFF_MISC + 32);  // [4]
+  uint64_t* k_full = bars + 2;     // [2]
+  uint64_t* k_empty = bars + 4;    // [2]
+  uint64_t* v_full = bars + 6;     // [2]
+  uint64_t* v_empty = bars + 8;    // [2]
+  uint64_t* s_full = bars + 10;    // [2]
+  uint64_t* p_full = bars + 12;    // [2]
+  uint64_t* o_done = bars + 14;    // after every PV
+  uint64_t* o_final = bars + 15;   // after an item's last PV
+  uint64_t* o_free = bars + 16;    // the epilogue has read O
+  uint64_t* drain = bars + 17;
+  uint64_t* item_full = bars + 18;   // [4] ring of work items handed from the producer
+  uint64_t* item_empty = bars + 22;  // [4]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
-  int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);  // loads issued: [0] K, [1] V, [2] Q
+  int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);     // loads issued: [0] K, [1] V, [2] Q
+  int* item_ring = reinterpret_cast<int*>(smem + C::OFF_MISC + 32);  // [4]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.H / p.Hkv;
@@ -162,13 +162,16 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    mbar_init(k_full, 1);
-    mbar_init(k_empty, 1);
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(k_full + b, 1);
+      mbar_init(k_empty + b, 1);
+      mbar_init(v_full + b, 1);
+      mbar_init(v_empty + b, 1);
+      mbar_init(s_full + b, 1);
+      mbar_init(p_full + b, 128);
+    }
     mbar_init(o_done, 1);
+    mbar_init(o_final, 1);
     mbar_init(o_free, 128);
     mbar_init(drain, 1);
     for (int r = 0; r < 4; ++r) {
@@ -189,61 +192,54 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // The producer hands out work items: the block's first item is blockIdx.x,
-  // later ones come from an atomic counter (dynamic, longest-first order), and
-  // each is passed to the MMA and softmax warps through a 4-deep ring.  Every
-  // role counts KV tiles and items across items, so the single-buffer barriers
-  // keep alternating phases from one item to the next.
+  // Items reach the MMA and softmax warps through a 4-deep ring.  KV tiles are
+  // counted across items (g), so double-buffered barriers keep alternating
+  // phases from one item to the next: buffer g & 1, phase parity (g >> 1) & 1.
   auto take_item = [&](int k, uint32_t where) -> int {  // consumers: item k of this block, or -1
     if (!wait_bounded(item_full + (k & 3), (k >> 2) & 1, abort_flag, p.ws, where)) return -2;
     const int i = item_ring[k & 3];
     mbar_arrive(item_empty + (k & 3));
     return i;
   };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      int kc = 0, qc = 0;
+      int g = 0, qc = 0;
       bool ok = true;
       int i = blockIdx.x;
       for (int k = 0; ok; ++k) {
-        if (k >= 4 && !wait_bounded(item_empty + (k & 3), ((k >> 2) - 1) & 1, abort_flag, p.ws, 14)) break;
+        if (k >= 4 && !wait_bounded(item_empty + (k & 3), ((k >> 2) - 1) & 1, abort_flag, p.ws, 1)) break;
         item_ring[k & 3] = (i < n_items) ? i : -1;
         mbar_arrive(item_full + (k & 3));
         if (i >= n_items) break;
         const Item it = item_of(i, p.n_tiles, G);
-        const int n_kv = p.tiles[it.tile_id].n_kv_tiles;
+        const QTile tile = p.tiles[it.tile_id];
         i = (int)gridDim.x + (int)atomicAdd(&p.ws->next_item, 1u);
-        if (n_kv == 0) continue;
+        if (tile.n_kv_tiles == 0) continue;
         // Q of this item once every S MMA of the previous item has read its Q
-        if (qc > 0 && !wait_bounded(q_empty, (qc - 1) & 1, abort_flag, p.ws, 1)) break;
+        if (qc > 0 && !wait_bounded(q_empty, (qc - 1) & 1, abort_flag, p.ws, 2)) break;
         mbar_arrive_expect_tx(q_full, C::Q_BYTES);
         for (int kb = 0; kb < C::KB; ++kb)
-          tma_load_3d(smem + kb * C::BOX, &p.tm_q, q_full, kb * 64, it.h, p.tiles[it.tile_id].q_row0);
+          tma_load_3d(smem + kb * C::QBOX, &p.tm_q, q_full, kb * 64, it.h, tile.q_row0);
         issued[2] = ++qc;
-        PieceCursor c{p.tiles[it.tile_id].run_begin, 0, p.tiles[it.tile_id].run_end};
-        for (int j = 0; j < n_kv; ++j, ++kc) {
-          const Piece pa = c.next(p.runs);
-          const Piece pb = c.next(p.runs);
-          // an empty second piece reloads the first (finite values, masked out)
-          const int row_a = pa.row0, row_b = pb.len > 0 ? pb.row0 : pa.row0;
-          if (kc > 0 && !wait_bounded(k_empty, (kc - 1) & 1, abort_flag, p.ws, 2)) { ok = false; break; }
-          mbar_arrive_expect_tx(k_full, C::KV_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb) {
-            tma_load_3d(smem + C::OFF_K + kb * C::BOX, &p.tm_k, k_full, kb * 64, it.g, row_a);
-            tma_load_3d(smem + C::OFF_K + kb * C::BOX + C::BOX / 2, &p.tm_k, k_full, kb * 64, it.g, row_b);
-          }
-          issued[0] = kc + 1;
-          if (kc > 0 && !wait_bounded(v_empty, (kc - 1) & 1, abort_flag, p.ws, 3)) { ok = false; break; }
-          mbar_arrive_expect_tx(v_full, C::KV_BYTES);
-          for (int kb = 0; kb < C::KB; ++kb) {
-            tma_load_3d(smem + C::OFF_V + kb * C::BOX, &p.tm_v, v_full, kb * 64, it.g, row_a);
-            tma_load_3d(smem + C::OFF_V + kb * C::BOX + C::BOX / 2, &p.tm_v, v_full, kb * 64, it.g, row_b);
-          }
-          issued[1] = kc + 1;
+        PieceCursor c{tile.run_begin, 0, tile.run_end};
+        for (int j = 0; j < tile.n_kv_tiles; ++j, ++g) {
+          const int row = c.next(p.runs).row0;
+          const int b = g & 1;
+          if (g >= 2 && !wait_bounded(k_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 3)) { ok = false; break; }
+          mbar_arrive_expect_tx(k_full + b, C::KV_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(smem + C::OFF_K + b * C::KV_BYTES + kb * C::KVBOX, &p.tm_k, k_full + b, kb * 64, it.g, row);
+          issued[0] = g + 1;
+          if (g >= 2 && !wait_bounded(v_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 4)) { ok = false; break; }
+          mbar_arrive_expect_tx(v_full + b, C::KV_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_3d(smem + C::OFF_V + b * C::KV_BYTES + kb * C::KVBOX, &p.tm_v, v_full + b, kb * 64, it.g, row);
+          issued[1] = g + 1;
         }
       }
     }
@@ -251,50 +247,63 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      auto issue_s = [&]() {
+      // S_g = Q K_g^T into S buffer g & 1
+      auto issue_s = [&](int gg) {
+        const uint32_t kbase = sK + (gg & 1) * C::KV_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::BOX + (kk & 3) * 32;
-          umma_bf16_ss(tmem + C::TM_S, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
-                       IDESC_S, kk > 0 ? 1u : 0u);
+          const uint32_t qoff = (kk >> 2) * C::QBOX + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * C::KVBOX + (kk & 3) * 32;
+          umma_bf16_ss(tmem + C::TM_S + 64u * (gg & 1), smem_desc_sw128(sQ + qoff, 16, 1024),
+                       smem_desc_sw128(kbase + koff, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
         }
       };
-      int kc = 0, qc = 0, oc = 0;
+      int g = 0, qc = 0, oc = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
-        const int i = take_item(k, 15);
+        const int i = take_item(k, 5);
         if (i < 0) break;
         const int n_kv = p.tiles[item_of(i, p.n_tiles, G).tile_id].n_kv_tiles;
         if (n_kv == 0) continue;
-        ok = wait_bounded(q_full, qc & 1, abort_flag, p.ws, 4) && wait_bounded(k_full, kc & 1, abort_flag, p.ws, 5);
+        ok = wait_bounded(q_full, qc & 1, abort_flag, p.ws, 6);
         if (!ok) break;
         ++qc;
-        tc_fence_after();
-        issue_s();
-        umma_commit(k_empty);
-        if (n_kv == 1) umma_commit(q_empty);
-        umma_commit(s_full);
-        for (int j = 0; j < n_kv; ++j, ++kc) {
-          ok = wait_bounded(p_full, kc & 1, abort_flag, p.ws, 6) && wait_bounded(v_full, kc & 1, abort_flag, p.ws, 7);
-          // the first PV of an item overwrites O: the previous item's epilogue must have read it
-          if (ok && j == 0 && oc > 0) ok = wait_bounded(o_free, (oc - 1) & 1, abort_flag, p.ws, 8);
+        // S for the item's first two tiles
+        for (int j = 0; ok && j < 2 && j < n_kv; ++j) {
+          const int gg = g + j;
+          ok = wait_bounded(k_full + (gg & 1), (gg >> 1) & 1, abort_flag, p.ws, 7);
           if (!ok) break;
           tc_fence_after();
+          issue_s(gg);
+          umma_commit(k_empty + (gg & 1));
+          if (j == n_kv - 1) umma_commit(q_empty);
+          umma_commit(s_full + (gg & 1));
+        }
+        for (int j = 0; ok && j < n_kv; ++j, ++g) {
+          const int b = g & 1;
+          ok = wait_bounded(p_full + b, (g >> 1) & 1, abort_flag, p.ws, 8) &&
+               wait_bounded(v_full + b, (g >> 1) & 1, abort_flag, p.ws, 9);
+          // the first PV of an item overwrites O: the previous item's epilogue must have read it
+          if (ok && j == 0 && oc > 0) ok = wait_bounded(o_free, (oc - 1) & 1, abort_flag, p.ws, 10);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t vbase = sV + b * C::KV_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA: P columns 8kk.., V rows 16kk..
-            umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 8 * kk, smem_desc_sw128(sV + kk * 2048, C::BOX, 1024),
-                         IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(v_empty);
-          if (j + 1 < n_kv) {
-            ok = wait_bounded(k_full, (kc + 1) & 1, abort_flag, p.ws, 9);
+          for (int kk = 0; kk < 4; ++kk)  // 16 keys per MMA: P columns 8kk.., V rows 16kk..
+            umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 64u * b + 8 * kk,
+                         smem_desc_sw128(vbase + kk * 2048, C::KVBOX, 1024), IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(v_empty + b);
+          umma_commit(o_done);
+          if (j == n_kv - 1) umma_commit(o_final);
+          if (j + 2 < n_kv) {
+            const int gg = g + 2;
+            ok = wait_bounded(k_full + b, (gg >> 1) & 1, abort_flag, p.ws, 11);
             if (!ok) break;
             tc_fence_after();
-            issue_s();
-            umma_commit(k_empty);
-            if (j + 2 == n_kv) umma_commit(q_empty);
-            umma_commit(s_full);
-          } else {
-            umma_commit(o_done);
+            issue_s(gg);
+            umma_commit(k_empty + b);
+            if (j + 2 == n_kv - 1) umma_commit(q_empty);
+            umma_commit(s_full + b);
           }
         }
         ++oc;
@@ -309,48 +318,43 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
     const int row = quad * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
     const float c2 = p.scale_log2;
-    int kc = 0, oc = 0;
+    int g = 0, oc = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const int i = take_item(k, 16);
+      const int i = take_item(k, 12);
       if (!__all_sync(0xffffffffu, i != -2)) break;
       if (i < 0) break;
       const int tile_id = item_of(i, p.n_tiles, G).tile_id;
       const int n_kv = p.tiles[tile_id].n_kv_tiles;
+      const int q_pos = p.tiles[tile_id].q_pos0 + row;
       const int q_pos0 = p.tiles[tile_id].q_pos0;
       float m_ref = -INFINITY, l = 0.f;
       PieceCursor cur{p.tiles[tile_id].run_begin, 0, p.tiles[tile_id].run_end};
-      for (int j = 0; j < n_kv; ++j, ++kc) {
-        const Piece pa = cur.next(p.runs);
-        const Piece pb = cur.next(p.runs);
-        const bool tile_mask = (pa.len < 64) || (pb.len < 64) || (pa.causal && pa.pos0 + 63 > q_pos0) ||
-                               (pb.causal && pb.pos0 + 63 > q_pos0);
+      for (int j = 0; j < n_kv; ++j, ++g) {
+        const Piece pc = cur.next(p.runs);
+        const bool tile_mask = (pc.len < 64) || (pc.causal && pc.pos0 + 63 > q_pos0);
+        const int b = g & 1;
 
-        if (!__all_sync(0xffffffffu, wait_bounded(s_full, kc & 1, abort_flag, p.ws, 10))) {
+        if (!__all_sync(0xffffffffu, wait_bounded(s_full + b, (g >> 1) & 1, abort_flag, p.ws, 13))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t sr[128];
-        tmem_ld128_wait(tl + C::TM_S, sr);
-
-        float s[128];
+        uint32_t sr[64];
+        tmem_ld64_wait(tl + C::TM_S + 64u * b, sr);
+        float s[64];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c]);
         if (tile_mask) {
-          // keys 0-63 come from piece a, 64-127 from piece b: each is a prefix mask
-          int lim_a = pa.len, lim_b = pb.len;
-          if (pa.causal) lim_a = min(lim_a, q_pos0 + row - pa.pos0 + 1);
-          if (pb.causal) lim_b = min(lim_b, q_pos0 + row - pb.pos0 + 1);
+          int lim = pc.len;
+          if (pc.causal) lim = min(lim, q_pos - pc.pos0 + 1);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = (c < lim_a) ? s[c] : -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 64; ++c) s[64 + c] = (c < lim_b) ? s[64 + c] : -INFINITY;
+          for (int c = 0; c < 64; ++c) s[c] = (c < lim) ? s[c] : -INFINITY;
         }
         // row max: four chains of three-input max
         float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 128; c += 8) {
+        for (int c = 0; c < 64; c += 8) {
           m0 = fmax3(m0, s[c], s[c + 1]);
           m1 = fmax3(m1, s[c + 2], s[c + 3]);
           m2 = fmax3(m2, s[c + 4], s[c + 5]);
@@ -370,23 +374,26 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
         // exponents two at a time on the packed FP32 pipe: x = s*c2 - mc
         const float2 c2v = make_float2(c2, c2), nmc = make_float2(-mc, -mc);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        uint32_t pk[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const float2 x = __ffma2_rn(make_float2(s[64 * half + 2 * q], s[64 * half + 2 * q + 1]), c2v, nmc);
-            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            if (q & 1)
-              acc1 = __fadd2_rn(acc1, e);
-            else
-              acc0 = __fadd2_rn(acc0, e);
-            pk[q] = pack_bf16x2(e.x, e.y);
-          }
-          tmem_st32(tl + C::TM_S + 32u * half, pk);  // P over the first 64 columns of S
+        for (int q = 0; q < 32; ++q) {
+          const float2 x = __ffma2_rn(make_float2(s[2 * q], s[2 * q + 1]), c2v, nmc);
+          const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          if (q & 1)
+            acc1 = __fadd2_rn(acc1, e);
+          else
+            acc0 = __fadd2_rn(acc0, e);
+          pk[q] = pack_bf16x2(e.x, e.y);
         }
         l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        tmem_st32(tl + C::TM_S + 64u * b, pk);  // P over the first 32 columns of this S buffer
         if (__any_sync(0xffffffffu, scale_o)) {
+          // O may only be rescaled once PV_{g-1} (still in flight) has landed
+          if (!__all_sync(0xffffffffu, wait_bounded(o_done, (g - 1) & 1, abort_flag, p.ws, 14))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
           const float a = scale_o ? alpha : 1.f;
 #pragma unroll
           for (int cb = 0; cb < D / 32; ++cb) {
@@ -399,12 +406,12 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full);
+        mbar_arrive(p_full + b);
       }
       if (!ok) break;
 
       if (n_kv > 0) {
-        if (!__all_sync(0xffffffffu, wait_bounded(o_done, oc & 1, abort_flag, p.ws, 11))) break;
+        if (!__all_sync(0xffffffffu, wait_bounded(o_final, oc & 1, abort_flag, p.ws, 15))) break;
         tc_fence_after();
       }
       // epilogue: O / l and LSE at the output rows
@@ -459,8 +466,8 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
     // Let copies and MMAs already in flight land before the block exits.
     if (warp == 0 && lane == 0) {
       if (issued[2]) drain_wait(q_full, (issued[2] - 1) & 1);
-      if (issued[0]) drain_wait(k_full, (issued[0] - 1) & 1);
-      if (issued[1]) drain_wait(v_full, (issued[1] - 1) & 1);
+      for (int gg = max(0, issued[0] - 2); gg < issued[0]; ++gg) drain_wait(k_full + (gg & 1), (gg >> 1) & 1);
+      for (int gg = max(0, issued[1] - 2); gg < issued[1]; ++gg) drain_wait(v_full + (gg & 1), (gg >> 1) & 1);
     }
     __syncthreads();
   }

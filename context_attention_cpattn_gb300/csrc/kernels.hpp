@@ -32,11 +32,10 @@ struct AttnArgs {
   cudaStream_t stream = nullptr;
 };
 
-// q tile / kv piece sizes each attention kernel was built for.  The tensor-core
-// kernel's 128-key tile is two 64-key pieces, which may come from different
-// runs (short chunks share a tile).
+// q tile / KV tile sizes each attention kernel was built for ("pair": two
+// consecutive KV pieces form one kernel tile).
 constexpr int kTcTileM = 128, kTcTileN = 64;
-constexpr bool kTcPair = true;
+constexpr bool kTcPair = false;
 constexpr int kSimtTileM = 64, kSimtTileN = 32;
 constexpr bool kSimtPair = false;
 
