@@ -61,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--aux", action="store_true",
+                    help="time the HBM-bound kernels (merge, shard gather, loss norm) instead of the forward")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--rows", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -223,12 +225,16 @@ def cpu_baseline_child(args):
     w = inputs.workload(args.workload)
     q, k, v = inputs.make_qkv(w)
     cores = host_cores()
-    rows = inputs.sample_rows(w.T, max(8, args.rows or 64), seed=w.seed + 1)
+    n = max(8, args.rows or 64)
+    rows = inputs.sample_rows(w.T, n, seed=w.seed + 1)
     dt = oracle_rows(w, rows, q, k, v, cores)
-    if not args.rows:  # size the measured sample to the target duration
-        n = int(min(w.T, max(64, len(rows) * args.cpu_seconds / max(dt, 1e-3))))
-        rows = inputs.sample_rows(w.T, n, seed=w.seed + 2)
+    # grow the sample (at least doubling) until it takes about the target time
+    attempt = 0
+    while not args.rows and dt < 0.5 * args.cpu_seconds and n < w.T and attempt < 8:
+        n = int(min(w.T, n * max(2.0, args.cpu_seconds / max(dt, 1e-3))))
+        rows = inputs.sample_rows(w.T, n, seed=w.seed + 2 + attempt)
         dt = oracle_rows(w, rows, q, k, v, cores)
+        attempt += 1
     fl = row_flops(w.cu_seqlens, rows, w.H, w.D, w.causal)
     print(json.dumps({"value": fl / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                       "sample": f"{len(rows)} seeded query rows x {w.H} heads of {w.name} "
@@ -414,10 +420,85 @@ def run_ours(args, rep: Replicas):
     print(json.dumps(line), flush=True)
 
 
+def measured_hbm() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "of measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "of fallback"
+
+
+def run_aux(args):
+    """GB/s of the HBM-bound kernels on shapes of the workloads: the exact LSE
+    merge of cp=4 partials over the 32K micro-batch, the grid2d shard gather of
+    the 16x45x80 latent's Q, and the loss normalisation (micro-batch size and
+    a 64M-token vector).  Algorithmic bytes: everything read once + written once."""
+    import torch
+
+    import context_attention_cpattn_gb300 as cp
+    import inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, src = measured_hbm()
+    out = []
+
+    def timeit(fn, reps=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps / 1e3
+
+    def record(kernel, what, nbytes, sec):
+        gbs = nbytes / sec / 1e9
+        out.append({"kernel": kernel, "shape": what, "bytes": nbytes, "us": sec * 1e6, "GB_s": gbs,
+                    "frac": gbs / peak})
+
+    # merge: 4 partials x [32768, 32, 128] fp32 -> bf16 O and fp32 LSE
+    T, H, D, n = 32768, 32, 128, 4
+    g = torch.Generator(device=dev).manual_seed(1)
+    o_parts = [torch.randn(T, H, D, device=dev, generator=g) for _ in range(n)]
+    l_parts = [torch.randn(H, T, device=dev, generator=g) for _ in range(n)]
+    o = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(H, T, device=dev)
+    sec = timeit(lambda: cp.cpattn_merge(o_parts, l_parts, o, lse))
+    record("merge_kernel", "4 x [32768,32,128] fp32 -> bf16", n * (T * H * D * 4 + H * T * 4) + T * H * D * 2 + H * T * 4, sec)
+    del o_parts, l_parts, o, lse
+    # shard gather of the latent's Q rows (split_cp_2d)
+    w = inputs.workload("video_latent_grid2d")
+    plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
+    idx = torch.from_numpy(plan.index_map()).to(dev)
+    x = torch.randn(w.T, w.H, w.D, device=dev, generator=g).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    sec = timeit(lambda: cp.cpattn_gather_rows(x, y, idx))
+    record("permute_rows_kernel (gather)", "[57600,24,128] bf16", 2 * x.numel() * 2 + idx.numel() * 8, sec)
+    sec = timeit(lambda: cp.cpattn_scatter_rows(y, x, idx))
+    record("permute_rows_kernel (scatter)", "[57600,24,128] bf16", 2 * x.numel() * 2 + idx.numel() * 8, sec)
+    del x, y
+    # loss normalisation
+    res = torch.empty(1, dtype=torch.float64, device=dev)
+    cnt = torch.empty(1, dtype=torch.int64, device=dev)
+    for Tl in (32768, 1 << 26):
+        loss = torch.rand(Tl, device=dev, generator=g)
+        valid = (torch.rand(Tl, device=dev, generator=g) > 0.1).to(torch.uint8)
+        sec = timeit(lambda: cp.cpattn_token_loss_norm(loss, valid, res, cnt))
+        record("loss_norm_kernel", f"T={Tl}", Tl * 5, sec)
+    print(json.dumps({"aux": out, "hbm_peak_GB_s": peak, "peak_source": src}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.cpu_baseline_child:
         cpu_baseline_child(args)
+        return
+    if args.aux:
+        run_aux(args)
         return
     if args.impl == "reference":
         # host-only: rank 0 runs it, other ranks exit without work (no process group)
