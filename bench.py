@@ -489,7 +489,16 @@ def run_aux(args):
         valid = (torch.rand(Tl, device=dev, generator=g) > 0.1).to(torch.uint8)
         sec = timeit(lambda: cp.cpattn_token_loss_norm(loss, valid, res, cnt))
         record("loss_norm_kernel", f"T={Tl}", Tl * 5, sec)
-    print(json.dumps({"aux": out, "hbm_peak_GB_s": peak, "peak_source": src}), flush=True)
+    # Dynamic-CP solver (host C++): the micro-batch count sweep over a global
+    # batch of 2048 long-tailed samples, dp 8, pp 4, V 2, m = 4..16
+    rng = np.random.default_rng(3)
+    L = np.clip(np.exp(rng.normal(np.log(512), 1.2, 2048)), 64, 16384).astype(np.int64)
+    reps, t0 = 5, time.perf_counter()
+    for _ in range(reps):
+        r = cp.cpattn_dcp_sweep(L, 8, 4, 2, 4, 8, 16384, 4 * 128 * 32, 0)
+    host = [{"solver": "cpattn_dcp_sweep", "shape": "2048 samples, dp 8, pp 4, V 2, m 4..16 (13 schedules)",
+             "ms": (time.perf_counter() - t0) / reps * 1e3, "knee_m": r["knee_m"], "best_m": r["best_m"]}]
+    print(json.dumps({"aux": out, "host": host, "hbm_peak_GB_s": peak, "peak_source": src}), flush=True)
 
 
 def main(argv=None):

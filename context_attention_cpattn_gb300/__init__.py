@@ -44,6 +44,11 @@ class _PlanInfo(ctypes.Structure):
                 ("split_h", ctypes.c_int32), ("split_w", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+class _DcpConfig(ctypes.Structure):
+    _fields_ = [("max_cp", ctypes.c_int32), ("reserved", ctypes.c_int32), ("cap_tokens", ctypes.c_int64),
+                ("attn_coef", ctypes.c_int64), ("lin_coef", ctypes.c_int64)]
+
+
 _lib = None
 _P, _I32, _I64, _SZ, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
 
@@ -66,6 +71,9 @@ _SIGNATURES = {
     "cpattn_scatter_rows": [_P, _P, _I64, _P, _I64, _I64, _P],
     "cpattn_token_loss_norm": [_P, _P, _I64, _P, _P, _P, _P],
     "cpattn_fwd_flops": [_P, _I32, _I32, _I32, _I32, _P, _P],
+    "cpattn_dcp_quotas": [_P, _I32, _I32, _I32, ctypes.c_double, _P],
+    "cpattn_dcp_schedule": [_P, _I64, _P, _I32, _P, _P, _P, _P, _P],
+    "cpattn_dcp_sweep": [_P, _I64, _P, _I32, _I32, _I32, _I32, _P, _P, _P],
     "cpattn_sync_status": [_P, _P],
     "cpattn_last_error_string": [],
     "cpattn_version": [],
@@ -287,3 +295,58 @@ def cpattn_fwd_flops(cu_seqlens, H: int, D: int, causal: bool) -> int:
 
 def cpattn_sync_status(workspace=None, stream=None):
     _check(lib().cpattn_sync_status(_ptr(workspace), _stream(stream)))
+
+
+# ------------------------------------------------------ Dynamic-CP scheduler
+
+def _dcp_config(max_cp, cap_tokens, attn_coef, lin_coef):
+    return _DcpConfig(int(max_cp), 0, int(cap_tokens), int(attn_coef), int(lin_coef))
+
+
+def _seqlens(lengths):
+    return np.ascontiguousarray(np.asarray(lengths, dtype=np.int64))
+
+
+def cpattn_dcp_quotas(m, vpp: int, pp: int, total: float) -> np.ndarray:
+    """Per-micro-batch workload of each DP rank from its micro-batch count m[i] (Eq. 1-3)."""
+    mm = np.ascontiguousarray(np.asarray(m, dtype=np.int32))
+    out = np.empty(len(mm), dtype=np.float64)
+    _check(lib().cpattn_dcp_quotas(mm.ctypes.data, len(mm), vpp, pp, float(total), out.ctypes.data))
+    return out
+
+
+def cpattn_dcp_schedule(lengths, n_micro: int, max_cp: int, cap_tokens: int, attn_coef: int, lin_coef: int = 0):
+    """Micro-batch and CP size of each sample, and each micro-batch's CP size, workload and tokens."""
+    L = _seqlens(lengths)
+    n = len(L)
+    cfg = _dcp_config(max_cp, cap_tokens, attn_coef, lin_coef)
+    out = {"sample_micro": np.empty(n, np.int32), "sample_cp": np.empty(n, np.int32),
+           "micro_cp": np.empty(n_micro, np.int32), "micro_work": np.empty(n_micro, np.int64),
+           "micro_tokens": np.empty(n_micro, np.int64)}
+    _check(lib().cpattn_dcp_schedule(L.ctypes.data, n, ctypes.byref(cfg), n_micro,
+                                     *[out[k].ctypes.data for k in ("sample_micro", "sample_cp", "micro_cp",
+                                                                     "micro_work", "micro_tokens")]))
+    return out
+
+
+def cpattn_dcp_sweep(lengths, dp: int, pp: int, vpp: int, mult: int, max_cp: int, cap_tokens: int,
+                     attn_coef: int, lin_coef: int = 0):
+    """Budget curve over m = pp..mult*pp micro-batches per DP rank, its knee and the chosen m."""
+    L = _seqlens(lengths)
+    cfg = _dcp_config(max_cp, cap_tokens, attn_coef, lin_coef)
+    budgets = np.empty((mult - 1) * pp + 1, np.int64)
+    knee, best = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().cpattn_dcp_sweep(L.ctypes.data, len(L), ctypes.byref(cfg), dp, pp, vpp, mult,
+                                  budgets.ctypes.data, ctypes.byref(knee), ctypes.byref(best)))
+    return {"m": np.arange(pp, mult * pp + 1), "budgets": budgets, "knee_m": knee.value, "best_m": best.value}
+
+
+def dcp_micro_batches(lengths, schedule) -> list:
+    """Each micro-batch as (sample ids in ascending order, cu_seqlens, cp size), ready for cpattn_plan."""
+    L = _seqlens(lengths)
+    out = []
+    for b, cp in enumerate(schedule["micro_cp"]):
+        ids = np.flatnonzero(schedule["sample_micro"] == b)
+        cu = np.concatenate([[0], np.cumsum(L[ids])]).astype(np.int32)
+        out.append((ids, cu, int(cp)))
+    return out

@@ -280,6 +280,70 @@ cpattn_status_t cpattn_token_loss_norm(const float* loss, const uint8_t* valid, 
 cpattn_status_t cpattn_fwd_flops(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t H,
                                  int32_t D, int32_t causal, uint64_t* out_u64, double* out_f64);
 
+/* ------------------------------------------------- Dynamic-CP scheduler (host)
+ *
+ * Per-micro-batch CP size and packing of a global batch of variable-length
+ * samples ("Speeding up Variable-Length Training with Dynamic Context
+ * Parallelism and NVIDIA Megatron Core", data-scheduling section, Eq. 1-3, and
+ * the runtime section's grid search over the micro-batch count).  Host
+ * functions: no device memory, no stream.  A micro-batch's samples, packed in
+ * ascending sample order, give the cu_seqlens and its CP size the cp_size of
+ * cpattn_plan.
+ *
+ * Workload model: workload(S) = attn_coef * S(S+1)/2 + lin_coef * S (the
+ * O(S^2) attention and O(S) per-token parts; attn_coef = 4*D*H makes the first
+ * term the causal attention FLOP count); memory(S) = S tokens.
+ * Readings of the prose: every micro-batch has the quota
+ * Q = ceil(total / n_micro); a sample's CP size is the smallest power of two
+ * c <= max_cp with workload <= c*Q and S <= c*cap_tokens (else max_cp); the
+ * n_micro lowest-workload samples open one micro-batch each; every other
+ * sample, by descending workload, joins the micro-batch with the least
+ * per-GPU load after the placement, load = workload * (max_cp / cp), among
+ * those whose tokens stay <= cp * cap_tokens, else the least-loaded one; a
+ * micro-batch's CP size is the largest of its samples'; ties go to the lower
+ * index.  Integer arithmetic throughout: results are exact and deterministic. */
+typedef struct cpattn_dcp_config {
+  int32_t max_cp;      /* largest CP group, a power of two in [1, 1024] */
+  int32_t reserved;    /* 0 */
+  int64_t cap_tokens;  /* activation memory cap: tokens one GPU holds (>= 1) */
+  int64_t attn_coef;   /* workload units per causal (query, key) pair (>= 0) */
+  int64_t lin_coef;    /* workload units per token (>= 0) */
+} cpattn_dcp_config_t;
+
+/* Eq. 1-3: per-micro-batch workload W_i of DP rank i with m[i] micro-batches,
+ * V = vpp virtual stages and p = pp pipeline stages, such that
+ * W_i (m_i V + p - 1) is the same on every rank and sum_i W_i m_i = total.
+ *   m: host int32 [dp] (each >= 1); w_out: host fp64 [dp].
+ *   Errors: CPATTN_INVALID_ARG for dp, vpp or pp < 1, m[i] < 1, or a negative
+ *   or non-finite total. */
+cpattn_status_t cpattn_dcp_quotas(const int32_t* m, int32_t dp, int32_t vpp, int32_t pp, double total,
+                                  double* w_out);
+
+/* Packs n samples into n_micro micro-batches and picks their CP sizes.
+ *   seqlens: host int64 [n], each in [1, 2^40].  Outputs (host, any may be
+ *   NULL): sample_micro [n] and sample_cp [n]; micro_cp, micro_work,
+ *   micro_tokens [n_micro] (a micro-batch with no sample has cp 1, work 0).
+ *   Errors: CPATTN_INVALID_ARG for a bad config, n_micro < 1, a length out of
+ *   range, or total workload * max_cp beyond int64. */
+cpattn_status_t cpattn_dcp_schedule(const int64_t* seqlens, int64_t n, const cpattn_dcp_config_t* cfg,
+                                    int32_t n_micro, int32_t* sample_micro, int32_t* sample_cp,
+                                    int32_t* micro_cp, int64_t* micro_work, int64_t* micro_tokens);
+
+/* Grid search over the micro-batch count m per DP rank (the same on every
+ * rank), m = pp .. mult*pp: budgets[m - pp] = the largest per-GPU load
+ * (workload * max_cp / cp) of cpattn_dcp_schedule with dp*m micro-batches.
+ * *knee_m = the knee of that curve: the m farthest below the chord from its
+ * first to its last point with both axes scaled to [0, 1] (the first m when
+ * the curve does not fall).  *best_m = the m in {knee-1, knee, knee+1} with
+ * the least Eq. 1 step time budget * (m*vpp + pp - 1) (the reading used in
+ * place of the pages' pipeline simulator).  Ties go to the smaller m.
+ *   budgets: host int64 [(mult-1)*pp + 1] or NULL; knee_m, best_m may be NULL.
+ *   Errors: CPATTN_INVALID_ARG as cpattn_dcp_schedule, or dp, pp, vpp,
+ *   mult < 1, or dp*mult*pp > 2^20. */
+cpattn_status_t cpattn_dcp_sweep(const int64_t* seqlens, int64_t n, const cpattn_dcp_config_t* cfg, int32_t dp,
+                                 int32_t pp, int32_t vpp, int32_t mult, int64_t* budgets, int32_t* knee_m,
+                                 int32_t* best_m);
+
 /* ----------------------------------------------------------------- helpers */
 
 /* Synchronise `stream`, then report a fault recorded by a kernel in

@@ -27,10 +27,14 @@ Contents and the passages each follows:
 * ``loss`` - per-token loss normalisation over valid tokens (Dynamic-CP
   article, section "Loss computation and FLOPS statistics").
 * ``flops`` - THD-aware FLOP count from real sequence lengths (same section).
+* ``dcp`` - the Dynamic-CP scheduler: Eq. 1-3 quotas, per-sample CP size,
+  packing into micro-batches and the micro-batch count sweep (Dynamic-CP
+  article, data-scheduling and runtime sections).
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against brute
-force, closed forms, library routines and invariants; no function is
-"parity unpinned".
+force, closed forms, library routines and invariants.  One exception is
+partial: ``dcp.schedule`` follows a prose heuristic, so past its invariants,
+bounds and a hand-worked case its parity is unpinned.
 """
 
-from . import attention, flops, loss, merge, plan  # noqa: F401
+from . import attention, dcp, flops, loss, merge, plan  # noqa: F401

@@ -127,3 +127,24 @@ def test_video_latent_grid2d_full_size(cp):
 
 def test_single_seq_1m_gqa_full_size(cp):
     _sampled(cp, "single_seq_1m_gqa", int(os.environ.get("CPATTN_1M_ROWS", "1024")))
+
+
+def test_dynamic_cp_micro_batches_each_at_their_own_cp_size(cp):
+    """A global batch packed by the Dynamic-CP scheduler: every micro-batch
+    runs the packed forward at the CP size chosen for it and matches the
+    oracle on all rows."""
+    rng = np.random.default_rng(5)
+    lengths = np.clip(np.exp(rng.normal(np.log(256), 1.0, 24)), 16, 2048).astype(np.int64)
+    sched = cp.cpattn_dcp_schedule(lengths, 4, 4, 1024, 4 * 128 * 4, 0)
+    sizes = set()
+    for ids, cu, cps in cp.dcp_micro_batches(lengths, sched):
+        if not len(ids):
+            continue
+        sizes.add(cps)
+        w = inputs.custom(tuple(int(x) for x in cu), 4, 2, 128, dtype="bf16", causal=True, mode="zigzag", cp=cps)
+        (q, k, v), (qd, kd, vd) = U.device_inputs(w)
+        plan = cp.cpattn_plan(cu, cps, "zigzag")
+        o, lse = U.run_fwd(cp, plan, w, qd, kd, vd)
+        O, L = A.packed_attention(q, k, v, w.cu_seqlens, True, w.scale)
+        U.check(o, lse, O, L, "bf16", f"dcp cp={cps}")
+    assert len(sizes) > 1      # the batch really mixes CP sizes

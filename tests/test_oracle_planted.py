@@ -93,3 +93,69 @@ def test_sdpa_pin_detects_missing_causal_mask():
     ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True, scale=0.4)
     assert np.abs(O_bidir[a:b] - ref[0].permute(1, 0, 2).numpy()).max() > 1e-3
     assert math.isfinite(float(ref.abs().max()))
+
+
+# ------------------------------------------------- Dynamic-CP scheduler slips
+
+def _run_pin(fn):
+    try:
+        fn()
+    except AssertionError:
+        return False
+    return True
+
+
+def test_dcp_quota_sign_slip_is_caught(monkeypatch):
+    import oracle.dcp as D
+    from tests import test_oracle_dcp as T
+    monkeypatch.setattr(D, "quotas", lambda m, V, p, total: [
+        (total / sum(mi / (mi * V + p + 1) for mi in m)) / (mi * V + p + 1) for mi in m])  # p+1 for p-1
+    assert not _run_pin(T.test_quotas_hand_solved)
+
+
+def test_dcp_most_loaded_choice_is_caught(monkeypatch):
+    import oracle.dcp as D
+    from tests import test_oracle_dcp as T
+
+    def planted(lengths, n_buckets, max_cp, cap, ac, lc):
+        # one GPU per micro-batch, no memory limit (the Graham pin's setting),
+        # but each later sample joins the MOST loaded micro-batch
+        w = [D.workload(int(S), ac, lc) for S in lengths]
+        order = sorted(range(len(w)), key=lambda s: (w[s], s))
+        bucket, b_work = [-1] * len(w), [0] * n_buckets
+        for i, s in enumerate(order[:n_buckets]):
+            bucket[s] = i
+            b_work[i] += w[s]
+        for s in sorted(order[n_buckets:], key=lambda s: (-w[s], s)):
+            b = max(range(n_buckets), key=lambda b: (b_work[b], -b))
+            bucket[s] = b
+            b_work[b] += w[s]
+        return bucket, [1] * len(w), [1] * n_buckets, b_work, [0] * n_buckets
+
+    monkeypatch.setattr(D, "schedule", planted)
+    caught = [not _run_pin(lambda s=s: T.test_graham_bound_against_brute_force_optimum(s)) for s in range(8)]
+    assert any(caught)
+
+
+def test_dcp_dropped_memory_check_is_caught(monkeypatch):
+    import oracle.dcp as D
+    from tests import test_oracle_dcp as T
+    real = D.schedule
+    monkeypatch.setattr(D, "schedule", lambda lengths, nb, max_cp, cap, ac, lc:
+                        real(lengths, nb, max_cp, 10**18, ac, lc))
+    assert not _run_pin(T.test_hand_worked_schedule_memory_decides)
+
+
+def test_dcp_knee_axis_swap_is_caught(monkeypatch):
+    import oracle.dcp as D
+    from tests import test_oracle_dcp as T
+
+    def planted(budgets):  # the X and Y scalings swapped
+        X, Y = len(budgets) - 1, budgets[0] - budgets[-1]
+        if X <= 0 or Y <= 0:
+            return 0
+        score = [i * X + (budgets[i] - budgets[-1]) * Y for i in range(len(budgets))]
+        return min(range(len(budgets)), key=lambda i: (score[i], i))
+
+    monkeypatch.setattr(D, "knee", planted)
+    assert not _run_pin(T.test_knee_on_hand_made_curves)
