@@ -17,6 +17,10 @@ Contents and the passages each follows:
   training with parallelism", opening section).  Also the attention of a
   query-row set over a key-row set (one ring step's block, "Scaling video
   training with parallelism", section 2, Ring Attention).
+* ``attention_bwd`` - fp64 gradients dQ, dK, dV of the packed attention from
+  the chain rule, and one ring step's backward block using the final O and
+  LSE (the pages train with blockwise ring attention: "Scaling video training
+  with parallelism", section 2).
 * ``merge`` - the exact log-sum-exp merge of block partials.  The pages name
   blockwise attention with a KV ring but not the merge; the merge written
   here is the plain identity that recombines softmax partials exactly.
@@ -37,4 +41,4 @@ partial: ``dcp.schedule`` follows a prose heuristic, so past its invariants,
 bounds and a hand-worked case its parity is unpinned.
 """
 
-from . import attention, dcp, flops, loss, merge, plan  # noqa: F401
+from . import attention, attention_bwd, dcp, flops, loss, merge, plan  # noqa: F401

@@ -1,0 +1,101 @@
+"""fp64 gradients of packed softmax attention - the backward's definition.
+
+Test infrastructure only (see the package docstring).
+
+The pages train with this attention ("Scaling video training with
+parallelism", opening section and section 2, Ring Attention: blockwise
+attention with the KV blocks passed around a ring, forward and backward;
+Dynamic-CP article: post-training and pre-training), so the backward pass is
+the plain derivative of the forward of ``oracle.attention``.  With
+s_ij = scale q_i.k_j on allowed pairs, P_ij = exp(s_ij - lse_i) and
+O_i = sum_j P_ij v_j, for an upstream gradient dO the chain rule gives
+
+    dV_j   = sum_i P_ij dO_i
+    dP_ij  = dO_i . v_j
+    delta_i = sum_j P_ij dP_ij            (= dO_i . O_i)
+    dS_ij  = P_ij (dP_ij - delta_i)
+    dQ_i   = scale sum_j dS_ij k_j
+    dK_j   = scale sum_i dS_ij q_i
+
+where dK and dV of a KV head sum over the query heads that read it.  A row
+with no allowed key contributes nothing.  A ring step's backward block uses
+the final (merged) O and LSE of its query rows: P over the block's keys is
+exp(s - lse) with the full-row lse, so the block gradients of all ring steps
+add up to the full gradients.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from .attention import causal_visible, kv_head, packed_attention, seq_ids_and_positions, to_f64
+
+
+def _block_grads(Qh, Kg, Vg, dOh, lse, delta, allowed, scale):
+    """Gradients of one (query rows, key rows) block for one query head."""
+    S = scale * (Qh @ Kg.T)
+    with np.errstate(invalid="ignore", over="ignore"):
+        P = np.where(allowed, np.exp(S - lse[:, None]), 0.0)
+    P[~np.isfinite(lse)] = 0.0
+    dV = P.T @ dOh
+    dP = dOh @ Vg.T
+    dS = P * (dP - delta[:, None])
+    dQ = scale * (dS @ Kg)
+    dK = scale * (dS.T @ Qh)
+    return dQ, dK, dV
+
+
+def packed_attention_bwd(q, k, v, dout, cu_seqlens, causal: bool, scale: float):
+    """(dQ [T,H,D], dK [T,Hkv,D], dV [T,Hkv,D]) in fp64 from the definition:
+    the forward (O, LSE) is recomputed here by ``oracle.attention``."""
+    q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
+    T, H, D = q.shape
+    Hkv = k.shape[1]
+    O, LSE = packed_attention(q, k, v, cu_seqlens, causal, scale)
+    delta = np.einsum("thd,thd->ht", do, O)
+    dQ = np.zeros_like(q)
+    dK = np.zeros_like(k)
+    dV = np.zeros_like(v)
+    cu = [int(c) for c in cu_seqlens]
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        pos = np.arange(b - a)
+        allowed = causal_visible(pos[None, :], pos[:, None]) if causal else np.ones((b - a, b - a), bool)
+        for h in range(H):
+            g = kv_head(h, H, Hkv)
+            gq, gk, gv = _block_grads(q[a:b, h], k[a:b, g], v[a:b, g], do[a:b, h], LSE[h, a:b], delta[h, a:b],
+                                      allowed, scale)
+            dQ[a:b, h] += gq
+            dK[a:b, g] += gk
+            dV[a:b, g] += gv
+    return dQ, dK, dV
+
+
+def block_attention_bwd(q, k, v, dout, O, LSE, cu_seqlens, q_rows, kv_rows, causal: bool, scale: float):
+    """One ring step's backward block: the gradients that the query rows
+    ``q_rows`` send through the key rows ``kv_rows``, using the final O [T,H,D]
+    and LSE [H,T] of the whole forward.  Returns (dQ [len(q_rows),H,D],
+    dK [len(kv_rows),Hkv,D], dV [len(kv_rows),Hkv,D])."""
+    q, k, v, do, O, LSE = to_f64(q), to_f64(k), to_f64(v), to_f64(dout), to_f64(O), to_f64(LSE)
+    T, H, D = q.shape
+    Hkv = k.shape[1]
+    seq, pos = seq_ids_and_positions(cu_seqlens)
+    q_rows = np.asarray(q_rows, dtype=np.int64)
+    kv_rows = np.asarray(kv_rows, dtype=np.int64)
+    dQ = np.zeros((len(q_rows), H, D))
+    dK = np.zeros((len(kv_rows), Hkv, D))
+    dV = np.zeros((len(kv_rows), Hkv, D))
+    if len(q_rows) == 0 or len(kv_rows) == 0:
+        return dQ, dK, dV
+    allowed = seq[q_rows][:, None] == seq[kv_rows][None, :]
+    if causal:
+        allowed &= causal_visible(pos[kv_rows][None, :], pos[q_rows][:, None])
+    delta = np.einsum("thd,thd->ht", do[q_rows], O[q_rows])
+    for h in range(H):
+        g = kv_head(h, H, Hkv)
+        gq, gk, gv = _block_grads(q[q_rows, h], k[kv_rows, g], v[kv_rows, g], do[q_rows, h], LSE[h, q_rows],
+                                  delta[h], allowed, scale)
+        dQ[:, h] += gq
+        dK[:, g] += gk
+        dV[:, g] += gv
+    return dQ, dK, dV

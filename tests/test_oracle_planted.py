@@ -159,3 +159,41 @@ def test_dcp_knee_axis_swap_is_caught(monkeypatch):
 
     monkeypatch.setattr(D, "knee", planted)
     assert not _run_pin(T.test_knee_on_hand_made_curves)
+
+
+# ------------------------------------------------------------ backward slips
+
+def _bwd_pins_hold():
+    from tests import test_oracle_attention_bwd as T
+    ok = True
+    for case in T.CASES:
+        ok &= _run_pin(lambda c=case: T.test_matches_torch_autograd(c))
+    ok &= _run_pin(T.test_central_finite_differences)
+    return ok
+
+
+def _planted_block_grads(mistake):
+    def grads(Qh, Kg, Vg, dOh, lse, delta, allowed, scale):
+        S = scale * (Qh @ Kg.T)
+        with np.errstate(invalid="ignore", over="ignore"):
+            P = np.where(allowed, np.exp(S - lse[:, None]), 0.0)
+        P[~np.isfinite(lse)] = 0.0
+        dV = (P @ dOh) if mistake == "untransposed_dv" else P.T @ dOh
+        dP = dOh @ Vg.T
+        d = dP.sum(axis=1) if mistake == "unweighted_delta" else delta
+        dS = P * (dP - d[:, None])
+        dQ = scale * (dS @ Kg)
+        dK = (dS.T @ Qh) if mistake == "unscaled_dk" else scale * (dS.T @ Qh)
+        return dQ, dK, dV
+    return grads
+
+
+def test_real_backward_oracle_passes():
+    assert _bwd_pins_hold()
+
+
+@pytest.mark.parametrize("mistake", ["untransposed_dv", "unweighted_delta", "unscaled_dk"])
+def test_backward_slips_are_caught(monkeypatch, mistake):
+    import oracle.attention_bwd as Bw
+    monkeypatch.setattr(Bw, "_block_grads", _planted_block_grads(mistake))
+    assert not _bwd_pins_hold()
