@@ -66,6 +66,10 @@ _SIGNATURES = {
     "cpattn_fwd": [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _I32, _P, _P, _P, _SZ, _P],
     "cpattn_fwd_static": [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _I32, _P, _P, _P],
     "cpattn_block_fwd": [_P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _I32, _I32, _I32, _P, _P, _P, _SZ, _P],
+    "cpattn_bwd_workspace_size": [_P, _I32, _I32, _I32, _I32, _I32, _P],
+    "cpattn_bwd": [_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _I32, _P, _P, _P, _P, _SZ, _P],
+    "cpattn_block_bwd": [_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _I32, _I32, _I32, _P, _P, _P, _P,
+                         _SZ, _P],
     "cpattn_merge": [_I32, _P, _P, _I64, _I32, _I32, _P, _I64, _P, _I32, _P, _P],
     "cpattn_gather_rows": [_P, _I64, _P, _P, _I64, _I64, _P],
     "cpattn_scatter_rows": [_P, _P, _I64, _P, _I64, _I64, _P],
@@ -253,6 +257,34 @@ def cpattn_block_fwd(plan: Plan, q, k, v, o_partial, lse_partial, workspace, q_r
     _check(lib().cpattn_block_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), H, Hkv, D, scale,
                                   int(bool(causal)), int(q_rank), int(ring_step), _ptr(o_partial),
                                   _ptr(lse_partial), _ptr(workspace), workspace.numel(), _stream(stream)))
+
+
+def cpattn_bwd_workspace_size(plan: Plan, H: int, Hkv: int, D: int, dtype, causal: bool) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().cpattn_bwd_workspace_size(plan.handle, H, Hkv, D, _dtype_code_of(dtype), int(bool(causal)),
+                                           ctypes.byref(out)))
+    return int(out.value)
+
+
+def cpattn_bwd(plan: Plan, q, k, v, o, lse, dout, dq, dk, dv, workspace, scale: Optional[float] = None,
+               causal: bool = True, stream=None):
+    """Whole packed backward: dq [T,H,D], dk, dv [T,Hkv,D] in the input dtype."""
+    T, H, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    _check(lib().cpattn_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                            _dtype_code(q), H, k.shape[1], D, scale, int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
+                            _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def cpattn_block_bwd(plan: Plan, q, k, v, o, lse, dout, dq_acc, dk_acc, dv_acc, workspace, q_rank: int,
+                     ring_step: int, scale: Optional[float] = None, causal: bool = True, stream=None):
+    """One ring step of the backward, added to fp32 accumulators at global rows."""
+    T, H, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    _check(lib().cpattn_block_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                  _dtype_code(q), H, k.shape[1], D, scale, int(bool(causal)), q_rank, ring_step,
+                                  _ptr(dq_acc), _ptr(dk_acc), _ptr(dv_acc), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def cpattn_merge(o_parts: Sequence, lse_parts: Sequence, o_out, lse_out, out_rows=None, stream=None):

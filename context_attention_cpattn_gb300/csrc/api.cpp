@@ -179,6 +179,57 @@ cpattn_status_t prepare(const cpattn_plan_t* plan, const void* q, const void* k,
   return CPATTN_OK;
 }
 
+// Backward workspace: header | tiles | runs | -lse*log2(e) [H,T] | -delta [H,T] |
+// dQ accumulator fp32 [T,H,D] | (GRID2D: index map | Q | K | V | dO shards)
+struct BwdLayout {
+  size_t tiles = 0, runs = 0, nl2 = 0, nd = 0, dq = 0, idx = 0, q = 0, k = 0, v = 0, dout = 0, total = 0;
+};
+
+BwdLayout bwd_layout(const cpattn_plan_t& p, const WorkList& wl, int H, int Hkv, int D, size_t es) {
+  BwdLayout L;
+  size_t off = CPATTN_WS_HEADER_BYTES;
+  L.tiles = off;
+  off += align256(wl.tiles.size() * sizeof(QTile));
+  L.runs = off;
+  off += align256(wl.runs.size() * sizeof(KvRun));
+  L.nl2 = off;
+  off += align256((size_t)p.T * H * sizeof(float));
+  L.nd = off;
+  off += align256((size_t)p.T * H * sizeof(float));
+  L.dq = off;
+  off += align256((size_t)p.T * H * D * sizeof(float));
+  if (p.mode == CPATTN_MODE_GRID2D) {
+    L.idx = off;
+    off += align256((size_t)p.T * sizeof(int64_t));
+    L.q = off;
+    off += align256((size_t)p.T * H * D * es);
+    L.k = off;
+    off += align256((size_t)p.T * Hkv * D * es);
+    L.v = off;
+    off += align256((size_t)p.T * Hkv * D * es);
+    L.dout = off;
+    off += align256((size_t)p.T * H * D * es);
+  }
+  L.total = off;
+  return L;
+}
+
+void bwd_tile_sizes(cpattn_dtype_t dt, int* tk, int* tq) {
+  if (dt == CPATTN_DTYPE_BF16) {
+    *tk = cpattn::kBwdTcTileK;
+    *tq = cpattn::kBwdTcTileQ;
+  } else {
+    *tk = cpattn::kBwdSimtTileK;
+    *tq = cpattn::kBwdSimtTileQ;
+  }
+}
+
+cpattn_status_t check_bwd_shape(int D, cpattn_dtype_t dt) {
+  if (dt == CPATTN_DTYPE_BF16 && D != 128)
+    return fail(CPATTN_UNSUPPORTED, "the bf16 backward supports head dim D = 128 (fp32: 64 or 128)");
+  return CPATTN_OK;
+}
+
 }  // namespace
 
 namespace cpattn {
@@ -391,6 +442,141 @@ cpattn_status_t cpattn_block_fwd(const cpattn_plan_t* plan, const void* q, const
   if (ring_step < 0 || ring_step >= plan->cp) return fail(CPATTN_INVALID_ARG, "ring_step out of range");
   return run_attention(plan, q, k, v, dtype, H, Hkv, D, scale, causal, q_rank, ring_step, o_partial, lse_partial,
                        workspace, ws_bytes, stream);
+}
+
+cpattn_status_t cpattn_bwd_workspace_size(const cpattn_plan_t* plan, int32_t H, int32_t Hkv, int32_t D,
+                                          cpattn_dtype_t dtype, int32_t causal, size_t* bytes) {
+  if (!plan || !bytes) return fail(CPATTN_INVALID_ARG, "NULL argument");
+  cpattn_status_t s = check_shape(H, Hkv, D, dtype);
+  if (s == CPATTN_OK) s = check_bwd_shape(D, dtype);
+  if (s != CPATTN_OK) return s;
+  if (causal && plan->mode == CPATTN_MODE_GRID2D)
+    return fail(CPATTN_UNSUPPORTED, "causal masks are not defined for grid2d plans");
+  int tk, tq;
+  bwd_tile_sizes(dtype, &tk, &tq);
+  auto wl = cpattn::get_worklist_bwd(*const_cast<cpattn_plan_t*>(plan), causal != 0, tk, tq, -1, 0);
+  *bytes = bwd_layout(*plan, *wl, H, Hkv, D, elem_size(dtype)).total;
+  return CPATTN_OK;
+}
+
+static cpattn_status_t run_backward(const cpattn_plan_t* cplan, const void* q, const void* k, const void* v,
+                                    const void* o, const float* lse, const void* dout, cpattn_dtype_t dtype,
+                                    int32_t H, int32_t Hkv, int32_t D, float scale, int32_t causal, int q_rank,
+                                    int step, void* dq, void* dk, void* dv, void* workspace, size_t ws_bytes,
+                                    void* stream_ptr) {
+  cpattn_status_t s = prepare(cplan, q, k, v, dtype, H, Hkv, D, causal, workspace, ws_bytes);
+  if (s == CPATTN_OK) s = check_bwd_shape(D, dtype);
+  if (s != CPATTN_OK) return s;
+  if (!o || !lse || !dout) return fail(CPATTN_INVALID_ARG, "o, lse and dout must be device pointers");
+  if (!dq || !dk || !dv) return fail(CPATTN_INVALID_ARG, "dq, dk and dv must be device pointers");
+  if (!aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(CPATTN_INVALID_ARG, "o, dout, dq, dk, dv must be 16-byte aligned");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CPATTN_INVALID_ARG, "scale must be positive and finite");
+  cpattn_plan_t* plan = const_cast<cpattn_plan_t*>(cplan);
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  int tk, tq;
+  bwd_tile_sizes(dtype, &tk, &tq);
+  auto wl_all = cpattn::get_worklist_bwd(*plan, causal != 0, tk, tq, -1, 0);
+  const size_t es = elem_size(dtype);
+  const BwdLayout L = bwd_layout(*plan, *wl_all, H, Hkv, D, es);
+  if (ws_bytes < L.total)
+    return fail(CPATTN_WORKSPACE, "workspace too small: need " + std::to_string(L.total) + " bytes");
+  auto wl = (q_rank < 0) ? wl_all : cpattn::get_worklist_bwd(*plan, causal != 0, tk, tq, q_rank, step);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WsLayout WL;
+  WL.tiles = L.tiles;
+  WL.runs = L.tiles + align256(wl->tiles.size() * sizeof(QTile));
+  s = upload_worklist(plan, *wl, WL, ws, stream);
+  if (s != CPATTN_OK) return s;
+
+  cpattn::BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dout_rows = dout;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.lse_ld = plan->T;
+  a.rows_total = plan->T;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.scale = scale;
+  a.bf16 = (dtype == CPATTN_DTYPE_BF16);
+  a.tiles = reinterpret_cast<const QTile*>(ws + WL.tiles);
+  a.runs = reinterpret_cast<const KvRun*>(ws + WL.runs);
+  a.n_tiles = (int32_t)wl->tiles.size();
+  a.nl2 = reinterpret_cast<float*>(ws + L.nl2);
+  a.nd = reinterpret_cast<float*>(ws + L.nd);
+  a.ws = reinterpret_cast<WsHeader*>(ws);
+  a.stream = stream;
+  if (q_rank < 0) {
+    a.dq_acc = reinterpret_cast<float*>(ws + L.dq);
+    a.zero_dq = true;
+    a.accumulate = false;
+  } else {
+    a.dq_acc = static_cast<float*>(dq);
+    a.zero_dq = false;
+    a.accumulate = true;
+  }
+  a.dk = dk;
+  a.dv = dv;
+  if (plan->mode == CPATTN_MODE_GRID2D) {
+    // split_cp_2d of Q, K, V and dO; results go back to global rows through the index map
+    uint8_t* idx = ws + L.idx;
+    s = upload_index_map(plan, idx, stream);
+    if (s != CPATTN_OK) return s;
+    const int64_t* index = reinterpret_cast<const int64_t*>(idx);
+    cudaError_t e;
+    e = cpattn::launch_permute_rows(q, ws + L.q, index, plan->T, (int64_t)H * D * es, plan->T, false, stream);
+    if (e == cudaSuccess)
+      e = cpattn::launch_permute_rows(k, ws + L.k, index, plan->T, (int64_t)Hkv * D * es, plan->T, false, stream);
+    if (e == cudaSuccess)
+      e = cpattn::launch_permute_rows(v, ws + L.v, index, plan->T, (int64_t)Hkv * D * es, plan->T, false, stream);
+    if (e == cudaSuccess)
+      e = cpattn::launch_permute_rows(dout, ws + L.dout, index, plan->T, (int64_t)H * D * es, plan->T, false, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "shard gather");
+    a.q = ws + L.q;
+    a.k = ws + L.k;
+    a.v = ws + L.v;
+    a.dout_rows = ws + L.dout;
+    a.in_map = index;
+    a.out_map = index;
+  }
+  cudaError_t e = cpattn::launch_bwd_pre(a);
+  if (e != cudaSuccess) return cuda_fail(e, "backward pre kernel");
+  std::string err;
+  e = a.bf16 ? cpattn::launch_attn_bwd_bf16_tc(a, &err) : cpattn::launch_attn_bwd_fp32_simt(a, &err);
+  if (e != cudaSuccess) {
+    if (!err.empty()) return fail(CPATTN_INVALID_ARG, err);
+    return cuda_fail(e, "backward kernel launch");
+  }
+  if (q_rank < 0) {
+    e = cpattn::launch_bwd_post(a.dq_acc, dq, a.bf16, (int64_t)plan->T * H * D, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "backward post kernel");
+  }
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_bwd(const cpattn_plan_t* plan, const void* q, const void* k, const void* v, const void* o,
+                           const float* lse, const void* dout, cpattn_dtype_t dtype, int32_t H, int32_t Hkv,
+                           int32_t D, float scale, int32_t causal, void* dq, void* dk, void* dv, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  return run_backward(plan, q, k, v, o, lse, dout, dtype, H, Hkv, D, scale, causal, -1, 0, dq, dk, dv, workspace,
+                      ws_bytes, stream);
+}
+
+cpattn_status_t cpattn_block_bwd(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
+                                 const void* o, const float* lse, const void* dout, cpattn_dtype_t dtype, int32_t H,
+                                 int32_t Hkv, int32_t D, float scale, int32_t causal, int32_t q_rank,
+                                 int32_t ring_step, float* dq_acc, float* dk_acc, float* dv_acc, void* workspace,
+                                 size_t ws_bytes, void* stream) {
+  if (!plan) return fail(CPATTN_INVALID_ARG, "plan is NULL");
+  if (q_rank < 0 || q_rank >= plan->cp) return fail(CPATTN_INVALID_ARG, "q_rank out of range");
+  if (ring_step < 0 || ring_step >= plan->cp) return fail(CPATTN_INVALID_ARG, "ring_step out of range");
+  return run_backward(plan, q, k, v, o, lse, dout, dtype, H, Hkv, D, scale, causal, q_rank, ring_step, dq_acc,
+                      dk_acc, dv_acc, workspace, ws_bytes, stream);
 }
 
 cpattn_status_t cpattn_merge(int32_t n_partials, const float* const* o_parts_host, const float* const* lse_parts_host,

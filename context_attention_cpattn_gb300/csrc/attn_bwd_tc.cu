@@ -1,0 +1,699 @@
+// bf16 packed varlen attention backward on the 5th-generation tensor cores.
+//
+// The backward of blockwise ring attention ("Scaling video training with
+// parallelism", section 2, Ring Attention: KV blocks travel around the ring
+// while each rank works on its own queries): for the KV shard of virtual rank
+// k the gradients dK, dV gather contributions from the queries of rank
+// (k + t) mod cp at ring step t, and every query collects dQ from every KV
+// shard it sees.  With P = exp(s - lse) recomputed from the saved LSE and
+// delta = rowsum(dO * O):
+//     dV += P^T dO      dP = dO V^T      dS = P (dP - delta)
+//     dK += scale dS^T Q                  dQ += scale dS K
+//
+// A work item is one KV tile (128 keys of one sequence in one rank's shard)
+// of one KV head.  It walks, for each query head of the group, the query runs
+// that see it in ring order, 64 queries at a time; dK and dV stay in TMEM for
+// the whole item and are written once, and each piece's dQ leaves through
+// fp32 reductions into a global accumulator.
+//
+// Persistent blocks, one per SM (all 512 TMEM columns):
+//   TMEM  S^T[2] (2 x 64) | dP^T (64) | dQ^T (64) | dV (128) | dK (128)
+// Warp roles (320 threads):
+//   warp 0      producer: K and V per item, Q_j and dO_j per piece through a
+//               two-deep ring (TMA), and the piece's -lse*log2(e) and -delta
+//               (plain loads by the 32 lanes) into shared memory.
+//   warp 1      TMEM allocator and MMA issuer (one thread), per piece j:
+//                 S^T_j  = K Q_j^T   (M=128 keys, N=64, K=D)        SS
+//                 dP^T_j = V dO_j^T  (M=128, N=64, K=D)             SS
+//                 dV    += P^T_j dO_j (M=128, N=D, K=64)           TS, A = P^T from TMEM
+//                 S^T_{j+1} (into the other S buffer)
+//                 dK    += dS^T_j Q_j (M=128, N=D, K=64)           TS, A = dS^T from TMEM
+//                 dQ^T_j = K^T dS^T_j (M=D, N=64, K=128 keys)      SS, both MN-major
+//                 dP^T_{j+1}
+//   warps 2-5   one key per thread: P^T from S^T (exp2 with the saved LSE,
+//               causal mask from token positions), written back to TMEM as
+//               bf16; dS^T from dP^T, written to TMEM (for dK) and to shared
+//               memory (the B operand of dQ^T); at the end of the item dK and
+//               dV from TMEM to global memory.
+//   warps 6-9   one head-dim column per thread: read dQ^T_j from TMEM and add
+//               it to the fp32 dQ accumulator (coalesced red.global.add).
+//
+// Shared-memory operand layouts (SWIZZLE_128B, 1024-byte aligned atoms):
+//   K, V:    [128 keys][64 d] boxes.  K-major A of S^T / dP^T; K is also the
+//            MN-major A of dQ^T (M = d: 64-wide d blocks one box apart (LBO),
+//            8-key groups 1024 B apart (SBO)).
+//   Q_j, dO_j: [64 queries][64 d] boxes.  K-major B of S^T / dP^T, MN-major B
+//            of dK / dV (N = d).
+//   dS^T_j:  [128 keys][64 queries], written by the softmax warps with the
+//            same 128-byte swizzle; MN-major B of dQ^T (N = queries).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.hpp"
+
+namespace cpattn {
+
+using namespace dev;
+
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
+                          std::string* err);
+
+namespace {
+
+struct alignas(64) BwdParams {
+  CUtensorMap tm_k, tm_v;   // [rows, Hkv, D], 128-row boxes
+  CUtensorMap tm_q, tm_do;  // [rows, H, D], 64-row boxes
+  const QTile* tiles;       // KV tiles (key rows in q_row0 / q_pos0 / q_rows / out_row0)
+  const KvRun* runs;        // query runs
+  const float* nl2;         // [H, ld]: -lse * log2(e) (-inf for a row with no key)
+  const float* nd;          // [H, ld]: -delta
+  int64_t ld;
+  float* dq_acc;            // fp32 [*, H, D], accumulated
+  void* dk;                 // bf16 [*, Hkv, D] stored, or fp32 accumulated (kAccum)
+  void* dv;
+  const int64_t* out_map;   // optional: output row of a buffer row
+  WsHeader* ws;
+  int32_t n_tiles, H, Hkv;
+  float scale_log2;         // softmax scale * log2(e)
+  float scale;              // softmax scale (dS is scaled by it)
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int KB = D / 64;
+  static constexpr uint32_t KBOX = 128 * 128;  // 128 key rows x 128 bytes
+  static constexpr uint32_t QBOX = 64 * 128;   // 64 query rows x 128 bytes
+  static constexpr uint32_t KT_BYTES = KB * KBOX;
+  static constexpr uint32_t QT_BYTES = KB * QBOX;
+  static constexpr uint32_t DS_BYTES = 128 * 128;  // dS^T: 128 keys x 64 queries bf16
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = KT_BYTES;
+  static constexpr uint32_t OFF_Q = 2 * KT_BYTES;             // Q[2]
+  static constexpr uint32_t OFF_DO = OFF_Q + 2 * QT_BYTES;    // dO[2]
+  static constexpr uint32_t OFF_DS = OFF_DO + 2 * QT_BYTES;   // dS^T[2]
+  static constexpr uint32_t OFF_LD = OFF_DS + 2 * DS_BYTES;   // [2 stages][nl2 64 | nd 64] floats
+  static constexpr uint32_t OFF_BAR = OFF_LD + 1024;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;         // 27 mbarriers (216 bytes) below
+  static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;      // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 192, TM_DV = 256, TM_DK = 384;
+};
+
+// Walks the query runs of an item in pieces of up to 64 queries, once per
+// query head of the KV head's group.
+struct Piece {
+  int row0, pos0, len, causal, hq;
+};
+struct QCursor {
+  int r, off, r_begin, r_end, hq;
+  __device__ Piece next(const KvRun* runs) {
+    Piece pc{0, 0, 0, 0, hq};
+    const KvRun run = runs[r];
+    pc.row0 = run.kv_row0 + off;
+    pc.pos0 = run.kv_pos0 + off;
+    pc.len = min(64, run.kv_len - off);
+    pc.causal = run.causal;
+    off += 64;
+    if (off >= run.kv_len) {
+      off = 0;
+      if (++r >= r_end) {
+        r = r_begin;
+        ++hq;
+      }
+    }
+    return pc;
+  }
+};
+
+struct Item {
+  int tile_id, g;
+};
+__device__ __forceinline__ Item item_of(int i, int n_tiles) { return Item{i % n_tiles, i / n_tiles}; }
+
+template <int D, bool kAccum>
+__global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr uint32_t IDESC_ST = idesc_bf16_f32(128, 64, false, false);
+  constexpr uint32_t IDESC_KV = idesc_bf16_f32(128, D, false, true);
+  constexpr uint32_t IDESC_DQ = idesc_bf16_f32(D, 64, true, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* qd_full = bars + 2;    // [2] Q_j and dO_j landed
+  uint64_t* qd_empty = bars + 4;   // [2] every MMA of piece j has run (stage and dS^T buffer free)
+  uint64_t* ld_full = bars + 6;    // [2] -lse2 / -delta of piece j in shared memory
+  uint64_t* s_full = bars + 8;     // [2]
+  uint64_t* p_full = bars + 10;    // [2]
+  uint64_t* dp_full = bars + 12;
+  uint64_t* ds_full = bars + 13;
+  uint64_t* dq_full = bars + 14;
+  uint64_t* dq_free = bars + 15;
+  uint64_t* acc_done = bars + 16;  // the item's last dK / dV MMA has run
+  uint64_t* acc_free = bars + 17;  // the epilogue has read dK / dV
+  uint64_t* drain = bars + 18;
+  uint64_t* item_full = bars + 19;   // [4]
+  uint64_t* item_empty = bars + 23;  // [4]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+  int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);     // loads issued: [0] K/V, [1] Q/dO
+  int* item_ring = reinterpret_cast<int*>(smem + C::OFF_MISC + 32);  // [4]
+  float* ldv = reinterpret_cast<float*>(smem + C::OFF_LD);           // [2][128]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.H / p.Hkv;
+  const int n_items = p.n_tiles * p.Hkv;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(qd_full + b, 1);
+      mbar_init(qd_empty + b, 1);
+      mbar_init(ld_full + b, 32);
+      mbar_init(s_full + b, 1);
+      mbar_init(p_full + b, 128);
+    }
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(acc_free, 128);
+    mbar_init(drain, 1);
+    for (int r = 0; r < 4; ++r) {
+      mbar_init(item_full + r, 1);
+      mbar_init(item_empty + r, 257);  // MMA thread + 128 softmax + 128 dQ threads
+    }
+    *abort_flag = 0;
+    issued[0] = issued[1] = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto take_item = [&](int k, uint32_t where) -> int {
+    if (!wait_bounded(item_full + (k & 3), (k >> 2) & 1, abort_flag, p.ws, where)) return -2;
+    const int i = item_ring[k & 3];
+    mbar_arrive(item_empty + (k & 3));
+    return i;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (whole warp)
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_do);
+    }
+    int g = 0, kc = 0;
+    bool ok = true;
+    int i = blockIdx.x;
+    for (int k = 0; ok; ++k) {
+      if (k >= 4 &&
+          !__all_sync(0xffffffffu, wait_bounded(item_empty + (k & 3), ((k >> 2) - 1) & 1, abort_flag, p.ws, 1)))
+        break;
+      if (lane == 0) {
+        item_ring[k & 3] = (i < n_items) ? i : -1;
+        mbar_arrive(item_full + (k & 3));
+      }
+      if (i >= n_items) break;
+      const Item it = item_of(i, p.n_tiles);
+      const QTile tile = p.tiles[it.tile_id];
+      int nxt = 0;
+      if (lane == 0) nxt = (int)gridDim.x + (int)atomicAdd(&p.ws->next_item, 1u);
+      i = __shfl_sync(0xffffffffu, nxt, 0);
+      const int n = tile.n_kv_tiles * G;
+      if (n == 0) continue;
+      // K and V of this item once the previous item's MMAs are done with them
+      if (kc > 0 && !__all_sync(0xffffffffu, wait_bounded(kv_empty, (kc - 1) & 1, abort_flag, p.ws, 2))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(kv_full, 2 * C::KT_BYTES);
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_load_3d(smem + C::OFF_K + kb * C::KBOX, &p.tm_k, kv_full, kb * 64, it.g, tile.q_row0);
+          tma_load_3d(smem + C::OFF_V + kb * C::KBOX, &p.tm_v, kv_full, kb * 64, it.g, tile.q_row0);
+        }
+        issued[0] = kc + 1;
+      }
+      ++kc;
+      QCursor cur{tile.run_begin, 0, tile.run_begin, tile.run_end, 0};
+      for (int t = 0; t < n; ++t, ++g) {
+        const Piece pc = cur.next(p.runs);
+        const int h = it.g * G + pc.hq;
+        const int b = g & 1;
+        if (g >= 2 &&
+            !__all_sync(0xffffffffu, wait_bounded(qd_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 3))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(qd_full + b, 2 * C::QT_BYTES);
+          for (int kb = 0; kb < C::KB; ++kb) {
+            tma_load_3d(smem + C::OFF_Q + b * C::QT_BYTES + kb * C::QBOX, &p.tm_q, qd_full + b, kb * 64, h, pc.row0);
+            tma_load_3d(smem + C::OFF_DO + b * C::QT_BYTES + kb * C::QBOX, &p.tm_do, qd_full + b, kb * 64, h,
+                        pc.row0);
+          }
+          issued[1] = g + 1;
+        }
+        // the piece's -lse*log2(e) and -delta (columns past the piece: -inf and 0, so P = 0 there)
+        float* dst = ldv + b * 128;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          const int c = c0 + lane;
+          const bool in = c < pc.len;
+          const int64_t src = (int64_t)h * p.ld + pc.row0 + (in ? c : 0);
+          dst[c] = in ? p.nl2[src] : -INFINITY;
+          dst[64 + c] = in ? p.nd[src] : 0.f;
+        }
+        mbar_arrive(ld_full + b);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+      const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+      // X^T_g = A B_g^T with A = K or V (K-major), B_g = Q or dO of piece g (K-major)
+      auto issue_t = [&](uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * C::KBOX + (kk & 3) * 32;
+          const uint32_t boff = (kk >> 2) * C::QBOX + (kk & 3) * 32;
+          umma_bf16_ss(d_tmem, smem_desc_sw128(a_base + aoff, 16, 1024), smem_desc_sw128(b_base + boff, 16, 1024),
+                       IDESC_ST, kk > 0 ? 1u : 0u);
+        }
+      };
+      int g = 0, kc = 0, ac = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int i = take_item(k, 5);
+        if (i < 0) break;
+        const int n = p.tiles[item_of(i, p.n_tiles).tile_id].n_kv_tiles * G;
+        if (n == 0) continue;
+        ok = wait_bounded(kv_full, kc & 1, abort_flag, p.ws, 6);
+        if (!ok) break;
+        ++kc;
+        {
+          const int b = g & 1;
+          ok = wait_bounded(qd_full + b, (g >> 1) & 1, abort_flag, p.ws, 7);
+          if (!ok) break;
+          tc_fence_after();
+          issue_t(tmem + C::TM_S + 64u * b, sK, sQ + b * C::QT_BYTES);
+          umma_commit(s_full + b);
+          issue_t(tmem + C::TM_DP, sV, sDO + b * C::QT_BYTES);
+          umma_commit(dp_full);
+        }
+        for (int t = 0; ok && t < n; ++t, ++g) {
+          const int b = g & 1;
+          ok = wait_bounded(p_full + b, (g >> 1) & 1, abort_flag, p.ws, 8);
+          // the item's first dV / dK overwrite the accumulators: the previous epilogue must have read them
+          if (ok && t == 0 && ac > 0) ok = wait_bounded(acc_free, (ac - 1) & 1, abort_flag, p.ws, 9);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t qb = sQ + b * C::QT_BYTES, dob = sDO + b * C::QT_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO: 16 queries per MMA
+            umma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + 64u * b + 8 * kk,
+                         smem_desc_sw128(dob + kk * 2048, C::QBOX, 1024), IDESC_KV, (t > 0 || kk > 0) ? 1u : 0u);
+          if (t + 1 < n) {
+            const int b1 = (g + 1) & 1;
+            ok = wait_bounded(qd_full + b1, ((g + 1) >> 1) & 1, abort_flag, p.ws, 10);
+            if (!ok) break;
+            tc_fence_after();
+            issue_t(tmem + C::TM_S + 64u * b1, sK, sQ + b1 * C::QT_BYTES);
+            umma_commit(s_full + b1);
+          }
+          ok = wait_bounded(ds_full, g & 1, abort_flag, p.ws, 11);
+          if (ok && g > 0) ok = wait_bounded(dq_free, (g - 1) & 1, abort_flag, p.ws, 12);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q
+            umma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + 8 * kk, smem_desc_sw128(qb + kk * 2048, C::QBOX, 1024),
+                         IDESC_KV, (t > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t dsb = sDS + b * C::DS_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T: 16 keys per MMA
+            umma_bf16_ss(tmem + C::TM_DQ, smem_desc_sw128(sK + kk * 2048, C::KBOX, 1024),
+                         smem_desc_sw128(dsb + kk * 2048, C::DS_BYTES, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
+          umma_commit(qd_empty + b);
+          umma_commit(dq_full);
+          if (t == n - 1) {
+            umma_commit(acc_done);
+            umma_commit(kv_empty);
+          } else {
+            const int b1 = (g + 1) & 1;
+            issue_t(tmem + C::TM_DP, sV, sDO + b1 * C::QT_BYTES);
+            umma_commit(dp_full);
+          }
+        }
+        ++ac;
+      }
+      umma_commit(drain);
+      drain_wait(drain, 0);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ P / dS (one key per thread) + epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+    const float c2 = p.scale_log2;
+    const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+    int g = 0, ac = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int i = take_item(k, 13);
+      if (!__all_sync(0xffffffffu, i != -2)) break;
+      if (i < 0) break;
+      const Item it = item_of(i, p.n_tiles);
+      const QTile tile = p.tiles[it.tile_id];
+      const int n = tile.n_kv_tiles * G;
+      const bool key_ok = row < tile.q_rows;
+      const int kp = tile.q_pos0 + row;
+      const int kp_last = tile.q_pos0 + tile.q_rows - 1;
+      QCursor cur{tile.run_begin, 0, tile.run_begin, tile.run_end, 0};
+      for (int t = 0; t < n; ++t, ++g) {
+        const Piece pc = cur.next(p.runs);
+        const int b = g & 1;
+        if (!__all_sync(0xffffffffu, wait_bounded(s_full + b, (g >> 1) & 1, abort_flag, p.ws, 14) &&
+                                         wait_bounded(ld_full + b, (g >> 1) & 1, abort_flag, p.ws, 15))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float* nl2 = ldv + b * 128;
+        const float* nd = nl2 + 64;
+        float P[64];
+        {
+          uint32_t sr[64];
+          tmem_ld64_wait(tl + C::TM_S + 64u * b, sr);
+          const float2 c2v = make_float2(c2, c2);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1])), c2v,
+                                        make_float2(nl2[2 * q], nl2[2 * q + 1]));
+            P[2 * q] = ex2_approx(x.x);
+            P[2 * q + 1] = ex2_approx(x.y);
+          }
+        }
+        if (!key_ok) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) P[c] = 0.f;
+        } else if (pc.causal && pc.pos0 < kp_last) {
+          const int lim = kp - pc.pos0;  // query column c sees this key iff c >= lim
+#pragma unroll
+          for (int c = 0; c < 64; ++c) P[c] = (c >= lim) ? P[c] : 0.f;
+        }
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) pk[q] = pack_bf16x2(P[2 * q], P[2 * q + 1]);
+          tmem_st32(tl + C::TM_S + 64u * b, pk);  // P^T over the first 32 columns of this S buffer
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full + b);
+
+        if (!__all_sync(0xffffffffu, wait_bounded(dp_full, g & 1, abort_flag, p.ws, 16))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t ds[32];
+        {
+          uint32_t dr[64];
+          tmem_ld64_wait(tl + C::TM_DP, dr);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const float a0 = P[2 * q] * p.scale * (__uint_as_float(dr[2 * q]) + nd[2 * q]);
+            const float a1 = P[2 * q + 1] * p.scale * (__uint_as_float(dr[2 * q + 1]) + nd[2 * q + 1]);
+            ds[q] = pack_bf16x2(a0, a1);
+          }
+        }
+        tmem_st32(tl + C::TM_DP, ds);  // dS^T (A of dK) over the first 32 columns of dP^T
+        // dS^T for dQ^T: this buffer was last read by the dQ^T MMA of piece g - 2
+        if (g >= 2 &&
+            !__all_sync(0xffffffffu, wait_bounded(qd_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 17))) {
+          ok = false;
+          break;
+        }
+        {
+          const uint32_t rbase = sDS + b * C::DS_BYTES + row * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(rbase + ((c ^ (row & 7)) << 4), ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+      }
+      if (!ok) break;
+
+      // epilogue: dK and dV of this KV tile
+      if (n > 0) {
+        if (!__all_sync(0xffffffffu, wait_bounded(acc_done, ac & 1, abort_flag, p.ws, 18))) break;
+        tc_fence_after();
+      }
+      const int64_t out_row = p.out_map ? p.out_map[tile.out_row0 + (key_ok ? row : 0)]
+                                        : (int64_t)tile.out_row0 + row;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        void* base = which ? p.dk : p.dv;
+        const uint32_t tcol = which ? C::TM_DK : C::TM_DV;
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t v[32];
+          if (n > 0) {
+            tmem_ld32_wait(tl + tcol + 32u * cb, v);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = 0u;
+          }
+          if (!key_ok) continue;
+          if (kAccum) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + (out_row * p.Hkv + it.g) * D + 32 * cb);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              float4 a = dst[q];
+              a.x += __uint_as_float(v[4 * q]);
+              a.y += __uint_as_float(v[4 * q + 1]);
+              a.z += __uint_as_float(v[4 * q + 2]);
+              a.w += __uint_as_float(v[4 * q + 3]);
+              dst[q] = a;
+            }
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + (out_row * p.Hkv + it.g) * D +
+                                                  32 * cb);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(
+                  pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                  pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                  pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                  pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+          }
+        }
+      }
+      if (n > 0) {
+        tc_fence_before();
+        mbar_arrive(acc_free);
+        ++ac;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ (one head-dim column per thread)
+    const int quad = warp & 3;
+    const int d = quad * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+    int g = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int i = take_item(k, 19);
+      if (!__all_sync(0xffffffffu, i != -2)) break;
+      if (i < 0) break;
+      const Item it = item_of(i, p.n_tiles);
+      const QTile tile = p.tiles[it.tile_id];
+      const int n = tile.n_kv_tiles * G;
+      QCursor cur{tile.run_begin, 0, tile.run_begin, tile.run_end, 0};
+      for (int t = 0; t < n; ++t, ++g) {
+        const Piece pc = cur.next(p.runs);
+        if (!__all_sync(0xffffffffu, wait_bounded(dq_full, g & 1, abort_flag, p.ws, 20))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v[64];
+        tmem_ld64_wait(tl + C::TM_DQ, v);
+        tc_fence_before();
+        mbar_arrive(dq_free);
+        if (d < D) {
+          const int h = it.g * G + pc.hq;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            if (c < pc.len) {
+              const int64_t r = p.out_map ? p.out_map[pc.row0 + c] : (int64_t)(pc.row0 + c);
+              atomicAdd(p.dq_acc + (r * p.H + h) * D + d, __uint_as_float(v[c]));
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    if (warp == 0 && lane == 0) {
+      if (issued[0]) drain_wait(kv_full, (issued[0] - 1) & 1);
+      for (int gg = max(0, issued[1] - 2); gg < issued[1]; ++gg) drain_wait(qd_full + (gg & 1), (gg >> 1) & 1);
+    }
+    __syncthreads();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// delta = rowsum(dO * O), -lse * log2(e) and (optionally) a zeroed dQ
+// accumulator row, one warp per (buffer row, head).  Rows of O, dO and LSE
+// are read at in_map[row] when a map is given (buffers of gathered shards).
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dout,
+                                                      const float* __restrict__ lse, int64_t lse_ld,
+                                                      const int64_t* __restrict__ in_map, int64_t rows, int H, int D,
+                                                      float* __restrict__ nl2, float* __restrict__ nd,
+                                                      float* __restrict__ dq_zero) {
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= rows * H) return;
+  const int64_t row = wid / H;
+  const int h = (int)(wid % H);
+  const int64_t src = in_map ? in_map[row] : row;
+  const T* orow = o + (src * H + h) * D;
+  const T* drow = dout + (src * H + h) * D;
+  float acc = 0.f;
+  for (int c = lane; c < D; c += 32) acc += (float)orow[c] * (float)drow[c];
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) {
+    const float l = lse[(int64_t)h * lse_ld + src];
+    nl2[(int64_t)h * rows + row] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+    nd[(int64_t)h * rows + row] = -acc;
+  }
+  if (dq_zero)
+    for (int c = lane; c < D; c += 32) dq_zero[(row * H + h) * D + c] = 0.f;
+}
+
+// dq[row] = dq_acc[row] in the output dtype (four elements per thread).
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float4* __restrict__ acc, T* __restrict__ dq, int64_t n4) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 a = acc[i];
+  if constexpr (sizeof(T) == 2) {
+    uint2 v = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+    reinterpret_cast<uint2*>(dq)[i] = v;
+  } else {
+    reinterpret_cast<float4*>(dq)[i] = a;
+  }
+}
+
+template <int D, bool kAccum>
+cudaError_t launch_bwd_tc(const BwdParams& p, int n_blocks, cudaStream_t stream) {
+  auto kern = attn_bwd_tc_kernel<D, kAccum>;
+  const uint32_t smem = BwdCfg<D>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<n_blocks, 320, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const BwdArgs& a) {
+  const int64_t warps = a.rows_total * a.H;
+  if (warps == 0) return cudaSuccess;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  if (a.bf16)
+    bwd_pre_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.lse_ld, a.in_map,
+        a.rows_total, a.H, a.D, a.nl2, a.nd, a.zero_dq ? a.dq_acc : nullptr);
+  else
+    bwd_pre_kernel<float><<<(unsigned)blocks, 256, 0, a.stream>>>(
+        static_cast<const float*>(a.o), static_cast<const float*>(a.dout), a.lse, a.lse_ld, a.in_map, a.rows_total,
+        a.H, a.D, a.nl2, a.nd, a.zero_dq ? a.dq_acc : nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, bool bf16, int64_t n, cudaStream_t stream) {
+  const int64_t n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  const int64_t blocks = (n4 + 255) / 256;
+  if (bf16)
+    bwd_post_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                                         static_cast<__nv_bfloat16*>(dq), n4);
+  else
+    bwd_post_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                                 static_cast<float*>(dq), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_bf16_tc(const BwdArgs& a, std::string* err) {
+  if (a.D != 128) {
+    *err = "the bf16 backward supports D = 128";
+    return cudaErrorInvalidValue;
+  }
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  if (!make_tensor_map_bf16(&p.tm_k, a.k, a.rows_total, a.Hkv, a.D, 128, err) ||
+      !make_tensor_map_bf16(&p.tm_v, a.v, a.rows_total, a.Hkv, a.D, 128, err) ||
+      !make_tensor_map_bf16(&p.tm_q, a.q, a.rows_total, a.H, a.D, 64, err) ||
+      !make_tensor_map_bf16(&p.tm_do, a.dout_rows, a.rows_total, a.H, a.D, 64, err))
+    return cudaErrorInvalidValue;
+  p.tiles = a.tiles;
+  p.runs = a.runs;
+  p.nl2 = a.nl2;
+  p.nd = a.nd;
+  p.ld = a.rows_total;
+  p.dq_acc = a.dq_acc;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.out_map = a.out_map;
+  p.ws = a.ws;
+  p.n_tiles = a.n_tiles;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  const int64_t items = (int64_t)a.n_tiles * a.Hkv;
+  if (items == 0) return cudaSuccess;
+  if (items > 0x7fffffff) {
+    *err = "too many KV tiles";
+    return cudaErrorInvalidValue;
+  }
+  const int64_t blocks = std::min<int64_t>(items, (int64_t)num_sms());
+  return a.accumulate ? launch_bwd_tc<128, true>(p, (int)blocks, a.stream)
+                      : launch_bwd_tc<128, false>(p, (int)blocks, a.stream);
+}
+
+}  // namespace cpattn

@@ -518,6 +518,11 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, 
   return true;
 }
 
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
+                          std::string* err) {
+  return make_map(m, base, rows, heads, D, box_rows, err);
+}
+
 template <int D, bool kPartial>
 static cudaError_t launch_tc(const TcParams& p, int n_blocks, cudaStream_t stream) {
   auto kern = attn_fwd_tc_kernel<D, kPartial>;

@@ -42,6 +42,45 @@ constexpr bool kSimtPair = false;
 cudaError_t launch_attn_bf16_tc(const AttnArgs& a, std::string* err);
 cudaError_t launch_attn_fp32_simt(const AttnArgs& a, std::string* err);
 
+// One backward launch over a backward work list (KV tiles with query runs).
+struct BwdArgs {
+  const void* q = nullptr;          // rows the kernel reads (gathered shards for GRID2D)
+  const void* k = nullptr;
+  const void* v = nullptr;
+  const void* dout_rows = nullptr;  // dO in the same row order as q
+  const void* o = nullptr;          // O and dO at global rows (read by the pre kernel through in_map)
+  const void* dout = nullptr;
+  const float* lse = nullptr;       // [H, lse_ld] at global rows
+  int64_t lse_ld = 0;
+  const int64_t* in_map = nullptr;  // buffer row -> global row, or null
+  int64_t rows_total = 0;
+  int32_t H = 0, Hkv = 0, D = 0;
+  float scale = 0.f;
+  bool bf16 = true;
+  const QTile* tiles = nullptr;     // device
+  const KvRun* runs = nullptr;      // device
+  int32_t n_tiles = 0;
+  float* nl2 = nullptr;             // scratch [H, rows_total]: -lse*log2(e)
+  float* nd = nullptr;              // scratch [H, rows_total]: -rowsum(dO*O)
+  float* dq_acc = nullptr;          // fp32 [*, H, D] at output rows, accumulated
+  bool zero_dq = false;             // the pre kernel clears dq_acc first
+  void* dk = nullptr;               // output dtype [*, Hkv, D] stored, or fp32 accumulated
+  void* dv = nullptr;
+  bool accumulate = false;
+  const int64_t* out_map = nullptr; // output row of a buffer row, or null
+  WsHeader* ws = nullptr;
+  cudaStream_t stream = nullptr;
+};
+
+// Backward tiles: KV tiles of kBwdTileK keys, query pieces of kBwdTileQ.
+constexpr int kBwdTcTileK = 128, kBwdTcTileQ = 64;
+constexpr int kBwdSimtTileK = 32, kBwdSimtTileQ = 64;
+
+cudaError_t launch_bwd_pre(const BwdArgs& a);
+cudaError_t launch_attn_bwd_bf16_tc(const BwdArgs& a, std::string* err);
+cudaError_t launch_attn_bwd_fp32_simt(const BwdArgs& a, std::string* err);
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, bool bf16, int64_t n, cudaStream_t stream);
+
 struct MergeArgs {
   int32_t n = 0;
   const float* o_parts[64] = {};

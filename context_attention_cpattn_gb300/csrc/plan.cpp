@@ -268,3 +268,85 @@ std::shared_ptr<const WorkList> get_worklist(cpattn_plan_t& p, bool causal, int 
 }
 
 }  // namespace cpattn
+
+namespace cpattn {
+
+static std::shared_ptr<WorkList> build_worklist_bwd(const cpattn_plan_t& p, bool causal, int tile_k, int tile_q,
+                                                    int q_rank, int step) {
+  auto wl = std::make_shared<WorkList>();
+  const int cp = p.cp;
+  const bool gathered = (p.mode == CPATTN_MODE_GRID2D);
+  std::vector<std::vector<Segment>> segs(cp);
+  for (int r = 0; r < cp; ++r) {
+    if (!gathered) {
+      segs[r] = p.rank_segments[r];
+    } else {
+      const int64_t a = p.rank_offsets[r], b = p.rank_offsets[r + 1];
+      if (b > a) segs[r].push_back({a, b - a, 0, a});
+    }
+  }
+  // KV ranks to visit, each with the ring steps (q ranks) that read it
+  for (int k = 0; k < cp; ++k) {
+    std::vector<int> q_ranks;
+    if (q_rank < 0) {
+      for (int t = 0; t < cp; ++t) q_ranks.push_back((k + t) % cp);
+    } else {
+      if (((q_rank - step) % cp + cp) % cp != k) continue;
+      q_ranks.push_back(q_rank);
+    }
+    for (const Segment& ks : segs[k]) {
+      for (int64_t off = 0; off < ks.len; off += tile_k) {
+        QTile t{};
+        const int64_t rows = std::min<int64_t>(tile_k, ks.len - off);
+        t.q_row0 = (int32_t)(ks.row0 + off);
+        t.q_pos0 = (int32_t)(ks.pos0 + off);
+        t.q_rows = (int32_t)rows;
+        t.out_row0 = t.q_row0;
+        t.rank = k;
+        t.run_begin = (int32_t)wl->runs.size();
+        const int64_t kp_first = ks.pos0 + off, kp_last = kp_first + rows - 1;
+        int64_t pieces = 0;
+        for (int r : q_ranks) {
+          const auto rng = seq_range(segs[r], ks.seq);
+          for (size_t i = rng.first; i < rng.second; ++i) {
+            const Segment& qs = segs[r][i];
+            int64_t q0 = qs.pos0, q1 = qs.pos0 + qs.len;  // query positions [q0, q1)
+            KvRun run{};
+            run.causal = 0;
+            if (causal) {
+              if (q1 - 1 < kp_first) continue;         // every query precedes the tile
+              q0 = std::max<int64_t>(q0, kp_first);    // queries before the first key see nothing
+              if (q0 < kp_last) run.causal = 1;        // some query precedes some key
+            }
+            run.kv_row0 = (int32_t)(qs.row0 + (q0 - qs.pos0));
+            run.kv_pos0 = (int32_t)q0;
+            run.kv_len = (int32_t)(q1 - q0);
+            wl->runs.push_back(run);
+            pieces += (run.kv_len + tile_q - 1) / tile_q;
+          }
+        }
+        t.run_end = (int32_t)wl->runs.size();
+        t.n_kv_tiles = (int32_t)pieces;
+        wl->total_kv_tiles += pieces;
+        wl->tiles.push_back(t);
+      }
+    }
+  }
+  std::stable_sort(wl->tiles.begin(), wl->tiles.end(),
+                   [](const QTile& a, const QTile& b) { return a.n_kv_tiles > b.n_kv_tiles; });
+  return wl;
+}
+
+std::shared_ptr<const WorkList> get_worklist_bwd(cpattn_plan_t& p, bool causal, int tile_k, int tile_q, int q_rank,
+                                                 int step) {
+  WorkKey key{causal ? 1 : 0, tile_k, tile_q, 0, q_rank, step};
+  key.bwd = 1;
+  std::lock_guard<std::mutex> lock(p.mu);
+  auto it = p.cache.find(key);
+  if (it != p.cache.end()) return it->second;
+  auto wl = build_worklist_bwd(p, causal, tile_k, tile_q, q_rank, step);
+  p.cache[key] = wl;
+  return wl;
+}
+
+}  // namespace cpattn

@@ -30,9 +30,10 @@ struct WorkList {
 
 struct WorkKey {
   int causal, tile_m, tile_n, pair, q_rank, step;  // q_rank = -1: every rank, every step
+  int bwd = 0;                                     // 1: backward work list (KV tiles with query runs)
   bool operator<(const WorkKey& o) const {
-    return std::tie(causal, tile_m, tile_n, pair, q_rank, step) <
-           std::tie(o.causal, o.tile_m, o.tile_n, o.pair, o.q_rank, o.step);
+    return std::tie(bwd, causal, tile_m, tile_n, pair, q_rank, step) <
+           std::tie(o.bwd, o.causal, o.tile_m, o.tile_n, o.pair, o.q_rank, o.step);
   }
 };
 
@@ -73,5 +74,17 @@ bool ring_entry(const cpattn_plan_t& p, int r, int t, bool causal, int32_t* kv_r
 // pieces (possibly from different runs) form one KV tile of the kernel.
 std::shared_ptr<const WorkList> get_worklist(cpattn_plan_t& p, bool causal, int tile_m, int tile_n, bool pair,
                                              int q_rank, int step);
+
+// Backward work list: the forward's pairs seen from the keys.  Each record of
+// `tiles` is a KV tile of up to tile_k consecutive key rows of one sequence
+// inside one rank's shard (q_row0/q_pos0/q_rows/out_row0 hold the key rows);
+// its runs list, in ring order, the query rows that see it: the KV shard of
+// rank k visits q rank (k + t) mod cp at ring step t.  A run starts at the
+// first query that sees the tile's first key (causal) and is flagged when some
+// of its queries precede some of the tile's keys.  n_kv_tiles holds the number
+// of tile_q-query pieces of the runs.  q_rank >= 0 keeps only the pairs of
+// ring step `step` of that q rank.
+std::shared_ptr<const WorkList> get_worklist_bwd(cpattn_plan_t& p, bool causal, int tile_k, int tile_q, int q_rank,
+                                                 int step);
 
 }  // namespace cpattn

@@ -198,6 +198,50 @@ cpattn_status_t cpattn_block_fwd(const cpattn_plan_t* plan, const void* q, const
                                  int32_t ring_step, float* o_partial, float* lse_partial,
                                  void* workspace, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- backward
+ *
+ * Gradients of the packed attention for an upstream gradient dO, computed the
+ * way blockwise ring attention trains ("Scaling video training with
+ * parallelism", section 2, Ring Attention): the KV shard of virtual rank k
+ * visits the query shards of ranks (k + t) mod cp at ring steps t = 0..cp-1,
+ * collecting dK and dV, while each query shard collects dQ.  Softmax
+ * probabilities are recomputed from the saved LSE:
+ *   P = exp(scale q.k - lse), delta = rowsum(dO * O),
+ *   dV = P^T dO,  dS = P * (dO V^T - delta),  dK = scale dS^T Q,  dQ = scale dS K
+ * (dK and dV of a KV head sum over the query heads that read it).
+ *   Supported: bf16 with D = 128 (tensor cores), fp32 with D = 64 or 128.
+ *   Other shapes: CPATTN_UNSUPPORTED.
+ *
+ * Workspace bytes for cpattn_bwd / cpattn_block_bwd with this plan and shape
+ * (work list, per-row scratch, a fp32 dQ accumulator [T,H,D], GRID2D shards). */
+cpattn_status_t cpattn_bwd_workspace_size(const cpattn_plan_t* plan, int32_t H, int32_t Hkv, int32_t D,
+                                          cpattn_dtype_t dtype, int32_t causal, size_t* bytes);
+
+/* The whole packed backward.
+ *   q, k, v, dout: device, the layouts of cpattn_fwd (dout like o);
+ *   o, lse: the forward's outputs for these inputs (cpattn_fwd).
+ *   dq [T,H,D], dk and dv [T,Hkv,D]: device outputs in the input dtype, every
+ *   row written.  Reads no output before writing it.
+ *   Errors as cpattn_fwd; CPATTN_WORKSPACE below cpattn_bwd_workspace_size. */
+cpattn_status_t cpattn_bwd(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
+                           const void* o, const float* lse, const void* dout, cpattn_dtype_t dtype,
+                           int32_t H, int32_t Hkv, int32_t D, float scale, int32_t causal, void* dq,
+                           void* dk, void* dv, void* workspace, size_t ws_bytes, void* stream);
+
+/* One ring step of the backward: the gradients that rank `q_rank`'s queries
+ * send through the KV shard of rank (q_rank - ring_step) mod cp, ADDED to
+ * fp32 accumulators at global rows:
+ *   dq_acc [T,H,D] += the step's dQ of rank q_rank's rows;
+ *   dk_acc, dv_acc [T,Hkv,D] += the step's dK, dV of the KV shard's rows.
+ * o and lse are the final (merged) forward outputs.  The cp steps of every
+ * rank add up to the gradients of cpattn_bwd (up to rounding).  Steps must not
+ * run concurrently on the same accumulators. */
+cpattn_status_t cpattn_block_bwd(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
+                                 const void* o, const float* lse, const void* dout, cpattn_dtype_t dtype,
+                                 int32_t H, int32_t Hkv, int32_t D, float scale, int32_t causal,
+                                 int32_t q_rank, int32_t ring_step, float* dq_acc, float* dk_acc,
+                                 float* dv_acc, void* workspace, size_t ws_bytes, void* stream);
+
 /* Exact log-sum-exp merge of n partials of the same rows:
  *   M = max_p lse_p;  lse = M + ln sum_p exp(lse_p - M);
  *   O = sum_p exp(lse_p - lse) * O_p.

@@ -48,7 +48,7 @@ DEFAULT_SEED = 20261202
 # PCG64 stream keyed by (seed, tensor id, block index).
 _BLOCK = 1 << 22
 
-_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "loss": 4, "lengths": 5, "valid": 6}
+_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "loss": 4, "lengths": 5, "valid": 6, "dout": 7}
 
 
 @dataclass(frozen=True)
@@ -241,6 +241,12 @@ def make_qkv(w: Workload, pin: bool = False):
     k = normal_tensor((w.T, w.Hkv, w.D), dt, w.seed, "k", w.value_scale, pin)
     v = normal_tensor((w.T, w.Hkv, w.D), dt, w.seed, "v", w.value_scale, pin)
     return q, k, v
+
+
+def make_dout(w: Workload, pin: bool = False):
+    """Host upstream gradient dO [T,H,D] for the backward: N(0,1) in the
+    workload dtype."""
+    return normal_tensor((w.T, w.H, w.D), w.torch_dtype, w.seed, "dout", 1.0, pin)
 
 
 def make_loss_inputs(w: Workload):

@@ -1,0 +1,141 @@
+"""GPU parity of the backward (cpattn_bwd and the per-step cpattn_block_bwd
+through the C ABI) against the fp64 backward oracle.
+
+Tolerances (derived from the arithmetic, written here): the bf16 kernel
+rounds P and dS to bf16 (relative 2^-9 per element) before the tensor-core
+products and reads the forward's bf16 O for delta, so each gradient carries
+a relative error of a few 1e-3; the bound is a per-head relative RMS of
+2e-2 on dQ, dK and dV plus a max-abs error of 5% of the tensor's largest
+magnitude.  fp32: 1e-5 of the largest magnitude."""
+
+import numpy as np
+import pytest
+import torch
+
+import inputs
+from oracle import attention_bwd as B
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+BWD_BF16_REL_RMS = 2e-2
+BWD_BF16_MAX = 5e-2
+BWD_FP32 = 1e-5
+
+
+@pytest.fixture(scope="module")
+def cp():
+    import context_attention_cpattn_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    m.build()
+    m.lib()
+    return m
+
+
+def check_grads(got, ref, dtype, where):
+    stats = {}
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        x = g.detach().to("cpu", torch.float64).numpy()
+        assert np.isfinite(x).all(), f"{where}: non-finite {name}"
+        err = np.abs(x - r)
+        scale = max(np.abs(r).max(initial=0), 1e-30)
+        stats[name + "_max_rel"] = float(err.max(initial=0) / scale)
+        if dtype == "bf16":
+            num = np.sqrt((err ** 2).sum(axis=(0, 2)))
+            den = np.sqrt((r ** 2).sum(axis=(0, 2)))
+            rel = num / np.maximum(den, 1e-30)
+            stats[name + "_rel_rms"] = float(rel.max(initial=0))
+            assert stats[name + "_rel_rms"] <= BWD_BF16_REL_RMS, (where, name, stats)
+            assert stats[name + "_max_rel"] <= BWD_BF16_MAX, (where, name, stats)
+        else:
+            assert stats[name + "_max_rel"] <= BWD_FP32, (where, name, stats)
+    print(where, stats)
+    return stats
+
+
+def _setup(cp, w):
+    (q, k, v), (qd, kd, vd) = U.device_inputs(w)
+    do = inputs.make_dout(w)
+    dod = do.cuda()
+    plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
+    o, lse = U.run_fwd(cp, plan, w, qd, kd, vd)
+    return (q, k, v, do), (qd, kd, vd, dod), plan, o, lse
+
+
+def _run_bwd(cp, plan, w, qd, kd, vd, o, lse, dod):
+    T, H, D = qd.shape
+    ws = torch.empty(cp.cpattn_bwd_workspace_size(plan, H, kd.shape[1], D, qd.dtype, w.causal), dtype=torch.uint8,
+                     device="cuda")
+    dq = torch.full_like(qd, float("nan"))
+    dk = torch.full_like(kd, float("nan"))
+    dv = torch.full_like(vd, float("nan"))
+    cp.cpattn_bwd(plan, qd, kd, vd, o, lse, dod, dq, dk, dv, ws, scale=w.scale, causal=w.causal)
+    cp.cpattn_sync_status(ws)
+    return dq, dk, dv
+
+
+SMALL = [
+    # cu_seqlens, H, Hkv, D, causal, mode, cp, grid
+    ((0, 300, 557), 2, 2, 128, True, "zigzag", 2, None),
+    ((0, 300, 557), 2, 2, 128, False, "zigzag", 2, None),
+    ((0, 4, 9, 300, 1111), 8, 2, 128, True, "zigzag", 2, None),
+    ((0, 700, 1500, 1501, 2600), 4, 1, 128, True, "contiguous", 3, None),
+    ((0, 777), 2, 2, 128, True, "zigzag", 1, None),
+    ((0, 2048), 2, 2, 128, True, "zigzag", 8, None),
+    ((0, 3 * 9 * 20), 2, 2, 128, False, "grid2d", 8, (3, 9, 20)),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"case{i}" for i in range(len(SMALL))])
+def test_bf16_backward_small_cases(cp, case):
+    cu, H, Hkv, D, causal, mode, cps, grid = case
+    w = inputs.custom(cu, H, Hkv, D, dtype="bf16", causal=causal, mode=mode, cp=cps, grid=grid)
+    (q, k, v, do), (qd, kd, vd, dod), plan, o, lse = _setup(cp, w)
+    got = _run_bwd(cp, plan, w, qd, kd, vd, o, lse, dod)
+    ref = B.packed_attention_bwd(q, k, v, do, cu, causal, w.scale)
+    check_grads(got, ref, "bf16", str(case))
+
+
+def test_bf16_backward_sharp_softmax(cp):
+    cu = (0, 513, 1400, 2048)
+    w = inputs.custom(cu, 4, 2, 128, dtype="bf16", causal=True, mode="zigzag", cp=4, value_scale=1.0)
+    (q, k, v, do), (qd, kd, vd, dod), plan, o, lse = _setup(cp, w)
+    got = _run_bwd(cp, plan, w, qd, kd, vd, o, lse, dod)
+    check_grads(got, B.packed_attention_bwd(q, k, v, do, cu, True, w.scale), "bf16", "sharp")
+
+
+@pytest.mark.parametrize("case", [((0, 64, 264, 520), 4, 4, 64, True, "zigzag", 2),
+                                  ((0, 100, 333), 4, 2, 128, False, "zigzag", 2),
+                                  ((0, 90, 200), 2, 1, 64, True, "contiguous", 3)])
+def test_fp32_backward(cp, case):
+    cu, H, Hkv, D, causal, mode, cps = case
+    w = inputs.custom(cu, H, Hkv, D, dtype="fp32", causal=causal, mode=mode, cp=cps)
+    (q, k, v, do), (qd, kd, vd, dod), plan, o, lse = _setup(cp, w)
+    got = _run_bwd(cp, plan, w, qd, kd, vd, o, lse, dod)
+    check_grads(got, B.packed_attention_bwd(q, k, v, do, cu, causal, w.scale), "fp32", str(case))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_block_backward_ring_steps_add_up(cp, dtype):
+    cu = (0, 300, 557, 1200)
+    w = inputs.custom(cu, 8, 2, 128, dtype=dtype, causal=True, mode="zigzag", cp=4)
+    (q, k, v, do), (qd, kd, vd, dod), plan, o, lse = _setup(cp, w)
+    T, H, D = qd.shape
+    ws = torch.empty(cp.cpattn_bwd_workspace_size(plan, H, 2, D, qd.dtype, True), dtype=torch.uint8, device="cuda")
+    dq = torch.zeros(T, H, D, dtype=torch.float32, device="cuda")
+    dk = torch.zeros(T, 2, D, dtype=torch.float32, device="cuda")
+    dv = torch.zeros(T, 2, D, dtype=torch.float32, device="cuda")
+    for r in range(w.cp):
+        for t in range(w.cp):
+            cp.cpattn_block_bwd(plan, qd, kd, vd, o, lse, dod, dq, dk, dv, ws, r, t, scale=w.scale, causal=True)
+            cp.cpattn_sync_status(ws)
+    ref = B.packed_attention_bwd(q, k, v, do, cu, True, w.scale)
+    check_grads((dq, dk, dv), ref, dtype, f"ring {dtype}")
+
+
+def test_backward_rejects_unsupported_shapes(cp):
+    plan = cp.cpattn_plan((0, 256), 2, "zigzag")
+    with pytest.raises(cp.CpattnError) as e:
+        cp.cpattn_bwd_workspace_size(plan, 2, 2, 64, torch.bfloat16, True)
+    assert e.value.status == cp.UNSUPPORTED
