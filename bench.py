@@ -63,6 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--aux", action="store_true",
                     help="time the HBM-bound kernels (merge, shard gather, loss norm) instead of the forward")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time the backward (cpattn_bwd) on the workload instead of the forward")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--rows", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -420,6 +422,67 @@ def run_ours(args, rep: Replicas):
     print(json.dumps(line), flush=True)
 
 
+def run_bwd(args):
+    """Backward on the workload: cpattn_bwd (delta/LSE prep, the tensor-core
+    kernel, dQ conversion) timed per call with CUDA events on its stream.
+    FLOPs = 2.5 x the forward's (five products of the forward's shape where
+    the forward has two), over valid (causal) pairs only."""
+    import torch
+
+    import context_attention_cpattn_gb300 as cp
+    import inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = inputs.workload(args.workload)
+    q_h, k_h, v_h = inputs.make_qkv(w)
+    qd, kd, vd = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    dod = inputs.make_dout(w).to(dev)
+    plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
+    fwd_flops = cp.cpattn_fwd_flops(w.cu_seqlens, w.H, w.D, w.causal)
+    flops = fwd_flops * 5 // 2
+    ws = torch.empty(max(cp.cpattn_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal),
+                         cp.cpattn_bwd_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal)),
+                     dtype=torch.uint8, device=dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.H, w.T), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cp.cpattn_fwd(plan, qd, kd, vd, o, lse, ws, scale=w.scale, causal=w.causal, stream=stream)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+
+    def step():
+        cp.cpattn_bwd(plan, qd, kd, vd, o, lse, dod, dq, dk, dv, ws, scale=w.scale, causal=w.causal, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    cp.cpattn_sync_status(ws, stream)
+    sampler = ClockSampler(0, os.path.join(ROOT, "gpurun_out", "clocks_bwd.csv")
+                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp/cpattn_clocks_bwd.csv")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    cp.cpattn_sync_status(ws, stream)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    mean_s = statistics.fmean(ms) / 1e3
+    peak, peak_src = measured_peak()
+    achieved = flops / mean_s / 1e12
+    launches = 3 + (4 if w.mode == "grid2d" else 0)
+    print(json.dumps({
+        "metric": "packed varlen attention bwd TFLOP/s (valid tokens, 2.5x forward FLOPs)", "value": achieved,
+        "unit": UNIT, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
+        "ms_min": min(ms), "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": config_of(w, flops),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "peak_source": peak_src, "traffic": None,
+                     "kernel": "cpattn_bwd call (pre + attn_bwd_tc_kernel + post), CUDA events per call"},
+        "gpu_launches": launches * args.steps, "clocks": clocks}), flush=True)
+
+
 def measured_hbm() -> tuple[float, str]:
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -508,6 +571,9 @@ def main(argv=None):
         return
     if args.aux:
         run_aux(args)
+        return
+    if args.bwd:
+        run_bwd(args)
         return
     if args.impl == "reference":
         # host-only: rank 0 runs it, other ranks exit without work (no process group)

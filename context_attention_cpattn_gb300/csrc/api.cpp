@@ -511,14 +511,17 @@ static cpattn_status_t run_backward(const cpattn_plan_t* cplan, const void* q, c
   a.nd = reinterpret_cast<float*>(ws + L.nd);
   a.ws = reinterpret_cast<WsHeader*>(ws);
   a.stream = stream;
-  if (q_rank < 0) {
+  // dQ accumulates at buffer rows: in the workspace (zeroed by the pre kernel)
+  // for the whole backward and for GRID2D steps, directly in the caller's
+  // accumulator for the other steps.
+  const bool grid2d = (plan->mode == CPATTN_MODE_GRID2D);
+  a.accumulate = (q_rank >= 0);
+  if (q_rank < 0 || grid2d) {
     a.dq_acc = reinterpret_cast<float*>(ws + L.dq);
     a.zero_dq = true;
-    a.accumulate = false;
   } else {
     a.dq_acc = static_cast<float*>(dq);
     a.zero_dq = false;
-    a.accumulate = true;
   }
   a.dk = dk;
   a.dv = dv;
@@ -552,8 +555,10 @@ static cpattn_status_t run_backward(const cpattn_plan_t* cplan, const void* q, c
     if (!err.empty()) return fail(CPATTN_INVALID_ARG, err);
     return cuda_fail(e, "backward kernel launch");
   }
-  if (q_rank < 0) {
-    e = cpattn::launch_bwd_post(a.dq_acc, dq, a.bf16, (int64_t)plan->T * H * D, stream);
+  if (q_rank < 0 || grid2d) {
+    // whole backward: dQ in the input dtype at global rows; GRID2D step: added to the caller's accumulator
+    e = cpattn::launch_bwd_post(a.dq_acc, dq, a.bf16, q_rank >= 0, plan->T, (int64_t)H * D,
+                                grid2d ? a.in_map : nullptr, stream);
     if (e != cudaSuccess) return cuda_fail(e, "backward post kernel");
   }
   return CPATTN_OK;

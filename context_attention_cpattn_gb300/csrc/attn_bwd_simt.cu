@@ -93,8 +93,7 @@ __global__ void __launch_bounds__(128) attn_bwd_simt_kernel(
           float acc = 0.f;
 #pragma unroll 8
           for (int kk = 0; kk < kKeys; ++kk) acc = fmaf(sds[kk], sK[kk][d], acc);
-          const int64_t orow = out_map ? out_map[qrow] : qrow;
-          atomicAdd(dq_acc + (orow * H + h) * D + d, acc);
+          atomicAdd(dq_acc + (qrow * H + h) * D + d, acc);
         }
       }
     }

@@ -35,8 +35,11 @@
 //               bf16; dS^T from dP^T, written to TMEM (for dK) and to shared
 //               memory (the B operand of dQ^T); at the end of the item dK and
 //               dV from TMEM to global memory.
-//   warps 6-9   one head-dim column per thread: read dQ^T_j from TMEM and add
-//               it to the fp32 dQ accumulator (coalesced red.global.add).
+//   warps 6-9   one head-dim column per thread: read dQ^T_j from TMEM into a
+//               [64 queries][D] fp32 tile in shared memory (two buffers); one
+//               thread adds the tile to the fp32 dQ accumulator with a TMA
+//               reduce-add (performed in L2).  Rows past the piece hold exact
+//               zeros (their dS is zero), so the whole 64-row box is added.
 //
 // Shared-memory operand layouts (SWIZZLE_128B, 1024-byte aligned atoms):
 //   K, V:    [128 keys][64 d] boxes.  K-major A of S^T / dP^T; K is also the
@@ -61,18 +64,20 @@ using namespace dev;
 
 bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
                           std::string* err);
+bool make_tensor_map_f32(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
+                         std::string* err);
 
 namespace {
 
 struct alignas(64) BwdParams {
   CUtensorMap tm_k, tm_v;   // [rows, Hkv, D], 128-row boxes
   CUtensorMap tm_q, tm_do;  // [rows, H, D], 64-row boxes
+  CUtensorMap tm_dq;        // fp32 dQ accumulator [rows, H, D], 64-row boxes, no swizzle
   const QTile* tiles;       // KV tiles (key rows in q_row0 / q_pos0 / q_rows / out_row0)
   const KvRun* runs;        // query runs
   const float* nl2;         // [H, ld]: -lse * log2(e) (-inf for a row with no key)
   const float* nd;          // [H, ld]: -delta
   int64_t ld;
-  float* dq_acc;            // fp32 [*, H, D], accumulated
   void* dk;                 // bf16 [*, Hkv, D] stored, or fp32 accumulated (kAccum)
   void* dv;
   const int64_t* out_map;   // optional: output row of a buffer row
@@ -96,8 +101,10 @@ struct BwdCfg {
   static constexpr uint32_t OFF_DO = OFF_Q + 2 * QT_BYTES;    // dO[2]
   static constexpr uint32_t OFF_DS = OFF_DO + 2 * QT_BYTES;   // dS^T[2]
   static constexpr uint32_t OFF_LD = OFF_DS + 2 * DS_BYTES;   // [2 stages][nl2 64 | nd 64] floats
-  static constexpr uint32_t OFF_BAR = OFF_LD + 1024;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;         // 27 mbarriers (216 bytes) below
+  static constexpr uint32_t DQS_BYTES = 64 * D * 4;          // dQ staging tile (fp32)
+  static constexpr uint32_t OFF_DQS = OFF_LD + 1024;          // dQ staging [2]
+  static constexpr uint32_t OFF_BAR = OFF_DQS + 2 * DQS_BYTES;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;         // 31 mbarriers (248 bytes) below
   static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;      // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 192, TM_DV = 256, TM_DK = 384;
@@ -161,6 +168,8 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
   uint64_t* drain = bars + 18;
   uint64_t* item_full = bars + 19;   // [4]
   uint64_t* item_empty = bars + 23;  // [4]
+  uint64_t* stage_full = bars + 27;  // [2] the dQ staging tile is written
+  uint64_t* stage_free = bars + 29;  // [2] its previous reduce has read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);     // loads issued: [0] K/V, [1] Q/dO
@@ -191,6 +200,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
     for (int r = 0; r < 4; ++r) {
       mbar_init(item_full + r, 1);
       mbar_init(item_empty + r, 257);  // MMA thread + 128 softmax + 128 dQ threads
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(stage_full + b, 128);
+      mbar_init(stage_free + b, 1);
     }
     *abort_flag = 0;
     issued[0] = issued[1] = 0;
@@ -521,7 +534,9 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
     // ------------------------------------------------------------ dQ (one head-dim column per thread)
     const int quad = warp & 3;
     const int d = quad * 32 + lane;
+    const bool leader = (warp == 6 && lane == 0);
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+    float* stage = reinterpret_cast<float*>(smem + C::OFF_DQS);
     int g = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -534,6 +549,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
       QCursor cur{tile.run_begin, 0, tile.run_begin, tile.run_end, 0};
       for (int t = 0; t < n; ++t, ++g) {
         const Piece pc = cur.next(p.runs);
+        const int sb = g & 1;
         if (!__all_sync(0xffffffffu, wait_bounded(dq_full, g & 1, abort_flag, p.ws, 20))) {
           ok = false;
           break;
@@ -543,18 +559,33 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
         tmem_ld64_wait(tl + C::TM_DQ, v);
         tc_fence_before();
         mbar_arrive(dq_free);
-        if (d < D) {
-          const int h = it.g * G + pc.hq;
+        // staging buffer sb: the reduce of piece g - 2 must have read it
+        if (leader) {
+          bulk_wait_group_read<1>();
+          mbar_arrive(stage_free + sb);
+        }
+        if (!__all_sync(0xffffffffu, wait_bounded(stage_free + sb, (g >> 1) & 1, abort_flag, p.ws, 21))) {
+          ok = false;
+          break;
+        }
+        float* st = stage + sb * (64 * D);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            if (c < pc.len) {
-              const int64_t r = p.out_map ? p.out_map[pc.row0 + c] : (int64_t)(pc.row0 + c);
-              atomicAdd(p.dq_acc + (r * p.H + h) * D + d, __uint_as_float(v[c]));
-            }
+        for (int c = 0; c < 64; ++c) st[c * D + d] = __uint_as_float(v[c]);
+        fence_proxy_async_smem();
+        mbar_arrive(stage_full + sb);
+        if (leader) {
+          if (!wait_bounded(stage_full + sb, (g >> 1) & 1, abort_flag, p.ws, 22)) {
+            ok = false;
+          } else {
+            tma_reduce_add_3d(&p.tm_dq, st, 0, it.g * G + pc.hq, pc.row0);
+            bulk_commit_group();
           }
         }
+        if (!__all_sync(0xffffffffu, ok)) break;
       }
     }
+    // every reduce has finished before the block exits
+    if (leader) bulk_wait_group_all();
   }
 
   // ------------------------------------------------------------ teardown
@@ -604,17 +635,29 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o, c
     for (int c = lane; c < D; c += 32) dq_zero[(row * H + h) * D + c] = 0.f;
 }
 
-// dq[row] = dq_acc[row] in the output dtype (four elements per thread).
-template <typename T>
-__global__ void __launch_bounds__(256) bwd_post_kernel(const float4* __restrict__ acc, T* __restrict__ dq, int64_t n4) {
+// From the fp32 dQ accumulator (buffer rows) to the output: row r goes to
+// map[r] (or r); kAdd adds to a fp32 output, else the value is stored in the
+// output dtype.  Four elements per thread.
+template <typename T, bool kAdd>
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float4* __restrict__ acc, T* __restrict__ out,
+                                                       int64_t n4, int64_t row4, const int64_t* __restrict__ map) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n4) return;
+  const int64_t row = i / row4, c = i - row * row4;
+  const int64_t dst = (map ? map[row] : row) * row4 + c;
   const float4 a = acc[i];
-  if constexpr (sizeof(T) == 2) {
-    uint2 v = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
-    reinterpret_cast<uint2*>(dq)[i] = v;
+  if constexpr (kAdd) {
+    float4* o = reinterpret_cast<float4*>(out) + dst;
+    float4 x = *o;
+    x.x += a.x;
+    x.y += a.y;
+    x.z += a.z;
+    x.w += a.w;
+    *o = x;
+  } else if constexpr (sizeof(T) == 2) {
+    reinterpret_cast<uint2*>(out)[dst] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
   } else {
-    reinterpret_cast<float4*>(dq)[i] = a;
+    reinterpret_cast<float4*>(out)[dst] = a;
   }
 }
 
@@ -645,16 +688,19 @@ cudaError_t launch_bwd_pre(const BwdArgs& a) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_post(const float* dq_acc, void* dq, bool bf16, int64_t n, cudaStream_t stream) {
-  const int64_t n4 = n / 4;
+cudaError_t launch_bwd_post(const float* dq_acc, void* out, bool out_bf16, bool add, int64_t rows,
+                            int64_t row_elems, const int64_t* map, cudaStream_t stream) {
+  const int64_t n4 = rows * row_elems / 4, row4 = row_elems / 4;
   if (n4 == 0) return cudaSuccess;
-  const int64_t blocks = (n4 + 255) / 256;
-  if (bf16)
-    bwd_post_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
-                                                                         static_cast<__nv_bfloat16*>(dq), n4);
+  const unsigned blocks = (unsigned)((n4 + 255) / 256);
+  const float4* acc = reinterpret_cast<const float4*>(dq_acc);
+  if (add)
+    bwd_post_kernel<float, true><<<blocks, 256, 0, stream>>>(acc, static_cast<float*>(out), n4, row4, map);
+  else if (out_bf16)
+    bwd_post_kernel<__nv_bfloat16, false><<<blocks, 256, 0, stream>>>(acc, static_cast<__nv_bfloat16*>(out), n4,
+                                                                      row4, map);
   else
-    bwd_post_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
-                                                                 static_cast<float*>(dq), n4);
+    bwd_post_kernel<float, false><<<blocks, 256, 0, stream>>>(acc, static_cast<float*>(out), n4, row4, map);
   return cudaGetLastError();
 }
 
@@ -668,14 +714,14 @@ cudaError_t launch_attn_bwd_bf16_tc(const BwdArgs& a, std::string* err) {
   if (!make_tensor_map_bf16(&p.tm_k, a.k, a.rows_total, a.Hkv, a.D, 128, err) ||
       !make_tensor_map_bf16(&p.tm_v, a.v, a.rows_total, a.Hkv, a.D, 128, err) ||
       !make_tensor_map_bf16(&p.tm_q, a.q, a.rows_total, a.H, a.D, 64, err) ||
-      !make_tensor_map_bf16(&p.tm_do, a.dout_rows, a.rows_total, a.H, a.D, 64, err))
+      !make_tensor_map_bf16(&p.tm_do, a.dout_rows, a.rows_total, a.H, a.D, 64, err) ||
+      !make_tensor_map_f32(&p.tm_dq, a.dq_acc, a.rows_total, a.H, a.D, 64, err))
     return cudaErrorInvalidValue;
   p.tiles = a.tiles;
   p.runs = a.runs;
   p.nl2 = a.nl2;
   p.nd = a.nd;
   p.ld = a.rows_total;
-  p.dq_acc = a.dq_acc;
   p.dk = a.dk;
   p.dv = a.dv;
   p.out_map = a.out_map;

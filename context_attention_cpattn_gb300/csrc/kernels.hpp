@@ -62,12 +62,12 @@ struct BwdArgs {
   int32_t n_tiles = 0;
   float* nl2 = nullptr;             // scratch [H, rows_total]: -lse*log2(e)
   float* nd = nullptr;              // scratch [H, rows_total]: -rowsum(dO*O)
-  float* dq_acc = nullptr;          // fp32 [*, H, D] at output rows, accumulated
+  float* dq_acc = nullptr;          // fp32 [rows_total, H, D] at buffer rows, accumulated
   bool zero_dq = false;             // the pre kernel clears dq_acc first
   void* dk = nullptr;               // output dtype [*, Hkv, D] stored, or fp32 accumulated
   void* dv = nullptr;
   bool accumulate = false;
-  const int64_t* out_map = nullptr; // output row of a buffer row, or null
+  const int64_t* out_map = nullptr; // output row of a buffer row for dK / dV, or null
   WsHeader* ws = nullptr;
   cudaStream_t stream = nullptr;
 };
@@ -79,7 +79,10 @@ constexpr int kBwdSimtTileK = 32, kBwdSimtTileQ = 64;
 cudaError_t launch_bwd_pre(const BwdArgs& a);
 cudaError_t launch_attn_bwd_bf16_tc(const BwdArgs& a, std::string* err);
 cudaError_t launch_attn_bwd_fp32_simt(const BwdArgs& a, std::string* err);
-cudaError_t launch_bwd_post(const float* dq_acc, void* dq, bool bf16, int64_t n, cudaStream_t stream);
+// dQ accumulator (fp32, buffer rows of row_elems values) to the output at
+// rows map[r] (or r): stored in the output dtype, or added to a fp32 output.
+cudaError_t launch_bwd_post(const float* dq_acc, void* out, bool out_bf16, bool add, int64_t rows,
+                            int64_t row_elems, const int64_t* map, cudaStream_t stream);
 
 struct MergeArgs {
   int32_t n = 0;

@@ -99,3 +99,37 @@ def block_attention_bwd(q, k, v, dout, O, LSE, cu_seqlens, q_rows, kv_rows, caus
         dK[:, g] += gk
         dV[:, g] += gv
     return dQ, dK, dV
+
+
+def dq_at_rows(q, k, v, dout, cu_seqlens, rows, causal: bool, scale: float):
+    """dQ [R,H,D] of the sampled query rows ``rows`` (all heads), each from
+    its full definition: the row's own forward (lse, O, delta) over its
+    sequence's allowed keys, then dS and dQ.  For sizes where the whole
+    backward is too large for the CPU."""
+    rows = np.asarray(rows, dtype=np.int64)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    H, D = q.shape[1], q.shape[2]
+    Hkv = k.shape[1]
+    seq = np.searchsorted(cu, rows, side="right") - 1
+    dQ = np.zeros((len(rows), H, D))
+    for s in np.unique(seq):
+        idx = np.nonzero(seq == s)[0]
+        a, b = int(cu[s]), int(cu[s + 1])
+        kend = int(rows[idx].max()) + 1 if causal else b
+        for g in range(Hkv):
+            Kg, Vg = to_f64(k[a:kend, g]), to_f64(v[a:kend, g])
+            for h in [h for h in range(H) if kv_head(h, H, Hkv) == g]:
+                Qr, dOr = to_f64(q[rows[idx], h]), to_f64(dout[rows[idx], h])
+                S = scale * (Qr @ Kg.T)
+                if causal:
+                    allowed = causal_visible(np.arange(kend - a)[None, :], (rows[idx] - a)[:, None])
+                    S = np.where(allowed, S, -np.inf)
+                m = S.max(axis=1, keepdims=True)
+                P = np.exp(S - m)
+                P /= P.sum(axis=1, keepdims=True)
+                O = P @ Vg
+                delta = np.sum(dOr * O, axis=1)
+                dP = dOr @ Vg.T
+                dS = P * (dP - delta[:, None])
+                dQ[idx, h] = scale * (dS @ Kg)
+    return dQ

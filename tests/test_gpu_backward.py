@@ -116,22 +116,26 @@ def test_fp32_backward(cp, case):
     check_grads(got, B.packed_attention_bwd(q, k, v, do, cu, causal, w.scale), "fp32", str(case))
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_block_backward_ring_steps_add_up(cp, dtype):
-    cu = (0, 300, 557, 1200)
-    w = inputs.custom(cu, 8, 2, 128, dtype=dtype, causal=True, mode="zigzag", cp=4)
+@pytest.mark.parametrize("dtype,mode", [("bf16", "zigzag"), ("fp32", "zigzag"), ("bf16", "grid2d")])
+def test_block_backward_ring_steps_add_up(cp, dtype, mode):
+    if mode == "grid2d":
+        cu, causal, grid = (0, 2 * 9 * 20), False, (2, 9, 20)
+    else:
+        cu, causal, grid = (0, 300, 557, 1200), True, None
+    w = inputs.custom(cu, 8, 2, 128, dtype=dtype, causal=causal, mode=mode, cp=4, grid=grid)
     (q, k, v, do), (qd, kd, vd, dod), plan, o, lse = _setup(cp, w)
     T, H, D = qd.shape
-    ws = torch.empty(cp.cpattn_bwd_workspace_size(plan, H, 2, D, qd.dtype, True), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(cp.cpattn_bwd_workspace_size(plan, H, 2, D, qd.dtype, causal), dtype=torch.uint8,
+                     device="cuda")
     dq = torch.zeros(T, H, D, dtype=torch.float32, device="cuda")
     dk = torch.zeros(T, 2, D, dtype=torch.float32, device="cuda")
     dv = torch.zeros(T, 2, D, dtype=torch.float32, device="cuda")
     for r in range(w.cp):
         for t in range(w.cp):
-            cp.cpattn_block_bwd(plan, qd, kd, vd, o, lse, dod, dq, dk, dv, ws, r, t, scale=w.scale, causal=True)
+            cp.cpattn_block_bwd(plan, qd, kd, vd, o, lse, dod, dq, dk, dv, ws, r, t, scale=w.scale, causal=causal)
             cp.cpattn_sync_status(ws)
-    ref = B.packed_attention_bwd(q, k, v, do, cu, True, w.scale)
-    check_grads((dq, dk, dv), ref, dtype, f"ring {dtype}")
+    ref = B.packed_attention_bwd(q, k, v, do, cu, causal, w.scale)
+    check_grads((dq, dk, dv), ref, dtype, f"ring {dtype} {mode}")
 
 
 def test_backward_rejects_unsupported_shapes(cp):
@@ -139,3 +143,43 @@ def test_backward_rejects_unsupported_shapes(cp):
     with pytest.raises(cp.CpattnError) as e:
         cp.cpattn_bwd_workspace_size(plan, 2, 2, 64, torch.bfloat16, True)
     assert e.value.status == cp.UNSUPPORTED
+
+
+def test_dynamic_cp_microbatch_backward_full_size(cp):
+    """The 32K-token micro-batch (H = 32, D = 128, zigzag cp = 4): dQ at every
+    chunk-boundary row plus 512 sampled rows from the oracle row by row; dK and
+    dV of every sequence of at most 2048 tokens from the full oracle; and on
+    every sequence and KV head the invariants sum_j dV_j = sum_i dO_i and
+    sum_j dK_j = 0 (relative to the summed magnitudes)."""
+    w = inputs.workload("dynamic_cp_microbatch")
+    (q, k, v, do), (qd, kd, vd, dod), plan, o, lse = _setup(cp, w)
+    dq, dk, dv = _run_bwd(cp, plan, w, qd, kd, vd, o, lse, dod)
+    cu = np.asarray(w.cu_seqlens)
+    rows = U.boundary_rows(plan, 512, w.T, seed=w.seed)
+    ref_dq = B.dq_at_rows(q, k, v, do, cu, rows, True, w.scale)
+    got_dq = dq[torch.from_numpy(rows).cuda()].to("cpu", torch.float64).numpy()
+    err = got_dq - ref_dq
+    rel = np.sqrt((err ** 2).sum(axis=(0, 2))) / np.sqrt((ref_dq ** 2).sum(axis=(0, 2)))
+    assert rel.max() <= BWD_BF16_REL_RMS, rel.max()
+    assert np.abs(err).max() <= BWD_BF16_MAX * np.abs(ref_dq).max()
+    dk64 = dk.to("cpu", torch.float64).numpy()
+    dv64 = dv.to("cpu", torch.float64).numpy()
+    do64 = do.to(torch.float64).numpy()
+    short = [s for s in range(len(cu) - 1) if cu[s + 1] - cu[s] <= 2048]
+    assert len(short) >= 5
+    for s in short:
+        a, b = int(cu[s]), int(cu[s + 1])
+        r_dq, r_dk, r_dv = B.packed_attention_bwd(q[a:b], k[a:b], v[a:b], do[a:b], (0, b - a), True, w.scale)
+        check_grads((dq[a:b], dk[a:b], dv[a:b]), (r_dq, r_dk, r_dv), "bf16", f"sequence {s} ({b - a} tokens)")
+    worst_v = worst_k = 0.0
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        for g in range(w.Hkv):
+            heads = [h for h in range(w.H) if h * w.Hkv // w.H == g]
+            lhs = dv64[a:b, g].sum(axis=0)
+            rhs = do64[a:b][:, heads].sum(axis=(0, 1))
+            worst_v = max(worst_v, np.linalg.norm(lhs - rhs) / np.sqrt((dv64[a:b, g] ** 2).sum() + 1e-30))
+            worst_k = max(worst_k, np.linalg.norm(dk64[a:b, g].sum(axis=0)) /
+                          np.sqrt((dk64[a:b, g] ** 2).sum() + 1e-30))
+    print("invariants: sum dV - sum dO", worst_v, "sum dK", worst_k)
+    assert worst_v <= 2e-2 and worst_k <= 2e-2

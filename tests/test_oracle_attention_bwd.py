@@ -127,3 +127,12 @@ def test_ring_steps_sum_to_the_full_gradients(mode, cp, causal, grid):
             acc[2][kr] += gv
     for a_, f_ in zip(acc, full):
         np.testing.assert_allclose(a_, f_, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_dq_at_rows_equals_the_full_backward(causal):
+    cu, H, Hkv, D = (0, 40, 41, 90), 4, 2, 8
+    q, k, v, do = _inputs(cu, H, Hkv, D, seed=8)
+    full = B.packed_attention_bwd(q, k, v, do, cu, causal, 0.35)[0]
+    rows = np.array([0, 5, 39, 40, 41, 77, 89])
+    np.testing.assert_allclose(B.dq_at_rows(q, k, v, do, cu, rows, causal, 0.35), full[rows], rtol=1e-11, atol=1e-13)
