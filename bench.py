@@ -49,6 +49,8 @@ DEFAULT_WORKLOAD = "dynamic_cp_microbatch"
 FALLBACK_BF16_TFLOPS = 1900.0
 TC_SOURCES = ("context_attention_cpattn_gb300/csrc/attn_tc.cu", "context_attention_cpattn_gb300/csrc/common.cuh")
 TRAFFIC_FILE = "profiles/attn_fwd_tc_dynamic_cp_microbatch.md"
+BWD_SOURCES = ("context_attention_cpattn_gb300/csrc/attn_bwd_tc.cu", "context_attention_cpattn_gb300/csrc/common.cuh")
+BWD_TRAFFIC_FILE = "profiles/attn_bwd_tc_dynamic_cp_microbatch.md"
 
 
 def parse_args(argv=None):
@@ -180,18 +182,18 @@ def measured_peak() -> tuple[float, str]:
         return FALLBACK_BF16_TFLOPS, "of fallback"
 
 
-def tc_source_hash() -> str:
+def tc_source_hash(sources=TC_SOURCES) -> str:
     h = hashlib.sha256()
-    for rel in TC_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source and this workload."""
-    path = os.path.join(ROOT, TRAFFIC_FILE)
+def recorded_traffic(workload: str, path=TRAFFIC_FILE, sources=TC_SOURCES):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if
+    the summary was taken on the current kernel source and this workload."""
+    path = os.path.join(ROOT, path)
     if workload != DEFAULT_WORKLOAD or not os.path.exists(path):
         return None
     vals = {}
@@ -199,7 +201,7 @@ def recorded_traffic(workload: str):
         if line.startswith("traffic_bytes_per_launch=") or line.startswith("source_sha256="):
             k, v = line.strip().split("=", 1)
             vals[k] = v
-    if vals.get("source_sha256") != tc_source_hash() or "traffic_bytes_per_launch" not in vals:
+    if vals.get("source_sha256") != tc_source_hash(sources) or "traffic_bytes_per_launch" not in vals:
         return None
     return float(vals["traffic_bytes_per_launch"])
 
@@ -478,7 +480,8 @@ def run_bwd(args):
         "ms_min": min(ms), "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": config_of(w, flops),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
-                     "peak_source": peak_src, "traffic": None,
+                     "peak_source": peak_src,
+                     "traffic": recorded_traffic(w.name, BWD_TRAFFIC_FILE, BWD_SOURCES),
                      "kernel": "cpattn_bwd call (pre + attn_bwd_tc_kernel + post), CUDA events per call"},
         "gpu_launches": launches * args.steps, "clocks": clocks}), flush=True)
 

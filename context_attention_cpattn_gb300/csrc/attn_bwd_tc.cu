@@ -49,11 +49,8 @@
 //            of dK / dV (N = d).
 //   dS^T_j:  [128 keys][64 queries], written by the softmax warps with the
 //            same 128-byte swizzle; MN-major B of dQ^T (N = queries).
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.hpp"
@@ -61,11 +58,6 @@
 namespace cpattn {
 
 using namespace dev;
-
-bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
-                          std::string* err);
-bool make_tensor_map_f32(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
-                         std::string* err);
 
 namespace {
 

@@ -41,11 +41,8 @@
 //         one box apart (LBO).
 // Items of one KV head are consecutive (all its query heads, query tiles
 // longest-first), so the KV rows the resident blocks stream stay in L2.
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.hpp"
@@ -480,72 +477,6 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
 
 // ------------------------------------------------------------------ host side
 
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// [rows, heads, D] bf16 viewed as a 3-D tensor (D, heads, rows); box = 64
-// columns x 1 head x box_rows rows (128 for Q, 64 for a K/V piece), 128-byte
-// swizzle.
-static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
-                     std::string* err) {
-  auto enc = tensor_map_encoder();
-  if (!enc) {
-    *err = "cuTensorMapEncodeTiled is not available from the driver";
-    return false;
-  }
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    *err = "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")";
-    return false;
-  }
-  return true;
-}
-
-bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
-                          std::string* err) {
-  return make_map(m, base, rows, heads, D, box_rows, err);
-}
-
-// [rows, heads, D] fp32 as (D, heads, rows); box = D columns x 1 head x
-// box_rows rows, no swizzle (the tile of a reduce-add from shared memory).
-bool make_tensor_map_f32(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
-                         std::string* err) {
-  auto enc = tensor_map_encoder();
-  if (!enc) {
-    *err = "cuTensorMapEncodeTiled is not available from the driver";
-    return false;
-  }
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)heads * D * 4};
-  cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)box_rows};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    *err = "cuTensorMapEncodeTiled (fp32) failed (" + std::to_string((int)r) + ")";
-    return false;
-  }
-  return true;
-}
-
 template <int D, bool kPartial>
 static cudaError_t launch_tc(const TcParams& p, int n_blocks, cudaStream_t stream) {
   auto kern = attn_fwd_tc_kernel<D, kPartial>;
@@ -559,9 +490,9 @@ static cudaError_t launch_tc(const TcParams& p, int n_blocks, cudaStream_t strea
 cudaError_t launch_attn_bf16_tc(const AttnArgs& a, std::string* err) {
   TcParams p;
   memset(&p, 0, sizeof(p));
-  if (!make_map(&p.tm_q, a.q, a.q_rows_total, a.H, a.D, 128, err) ||
-      !make_map(&p.tm_k, a.k, a.kv_rows_total, a.Hkv, a.D, 64, err) ||
-      !make_map(&p.tm_v, a.v, a.kv_rows_total, a.Hkv, a.D, 64, err))
+  if (!make_tensor_map_bf16(&p.tm_q, a.q, a.q_rows_total, a.H, a.D, 128, err) ||
+      !make_tensor_map_bf16(&p.tm_k, a.k, a.kv_rows_total, a.Hkv, a.D, 64, err) ||
+      !make_tensor_map_bf16(&p.tm_v, a.v, a.kv_rows_total, a.Hkv, a.D, 64, err))
     return cudaErrorInvalidValue;
   p.tiles = a.tiles;
   p.runs = a.runs;

@@ -1,6 +1,7 @@
 // Launch descriptors for the CUDA kernels (host side).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -108,5 +109,13 @@ cudaError_t launch_permute_rows(const void* src, void* dst, const int64_t* index
                                 int64_t row_bytes, int64_t other_rows, bool scatter, cudaStream_t stream);
 
 int num_sms();
+
+// TMA tensor maps of a [rows, heads, D] tensor viewed as (D, heads, rows):
+// bf16 with 64-column boxes and 128-byte swizzle, or fp32 with D-column boxes
+// and no swizzle.  On failure *err says why.
+bool make_tensor_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
+                          std::string* err);
+bool make_tensor_map_f32(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows,
+                         std::string* err);
 
 }  // namespace cpattn
