@@ -65,6 +65,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--aux", action="store_true",
                     help="time the HBM-bound kernels (merge, shard gather, loss norm) instead of the forward")
+    ap.add_argument("--mesh", default="",
+                    help="UxR: run the workload on the 2D-Attention mesh of U Ulysses x R ring virtual ranks")
     ap.add_argument("--bwd", action="store_true",
                     help="time the backward (cpattn_bwd) on the workload instead of the forward")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
@@ -314,7 +316,11 @@ def run_ours(args, rep: Replicas):
     loss_d, valid_d = loss_h.to(dev), valid_h.to(dev)
 
     t0 = time.perf_counter()
-    plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
+    if args.mesh:
+        u, r = (int(x) for x in args.mesh.lower().split("x"))
+        plan = cp.cpattn_plan_2d(w.cu_seqlens, u, r)
+    else:
+        plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
     ws_bytes = cp.cpattn_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal)
     plan_ms = 1e3 * (time.perf_counter() - t0)
     flops = cp.cpattn_fwd_flops(w.cu_seqlens, w.H, w.D, w.causal)
@@ -324,7 +330,9 @@ def run_ours(args, rep: Replicas):
     out_loss = torch.empty(1, dtype=torch.float64, device=dev)
     out_cnt = torch.empty(1, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 2 + (3 if w.mode == "grid2d" else 0)
+    # attention + loss; grid2d adds 3 shard gathers; the mesh adds 3 all-to-all gathers,
+    # the reverse all-to-all of O and the LSE regroup
+    launches_per_step = 2 + (5 if args.mesh else 3 if w.mode == "grid2d" else 0)
 
     def step(ev0=None, ev1=None):
         if ev0 is not None:
@@ -406,7 +414,8 @@ def run_ours(args, rep: Replicas):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": rep.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * elapsed_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_of(w, flops),
+        "config": dict(config_of(w, flops), **({"mode": "ulysses2d", "mesh": args.mesh + " (ulysses x ring)",
+                                                 "cp": plan.cp} if args.mesh else {})),
         "pct_of_bf16_peak": 100.0 * value / (peak * rep.world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
                      "peak_source": peak_src, "traffic": traffic,

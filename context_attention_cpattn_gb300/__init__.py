@@ -23,7 +23,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "cpattn.h")
 
 OK, INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA_ERROR, DEVICE_FAULT = range(6)
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA_ERROR", 5: "DEVICE_FAULT"}
-MODES = {"zigzag": 0, "grid2d": 1, "contiguous": 2}
+MODES = {"zigzag": 0, "grid2d": 1, "contiguous": 2, "ulysses2d": 3}
 DTYPE_FP32, DTYPE_BF16 = 0, 1
 MASK_SKIP, MASK_FULL, MASK_DIAG, MASK_KV_HEAD, MASK_Q_TAIL = range(5)
 
@@ -54,7 +54,9 @@ _P, _I32, _I64, _SZ, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, cty
 
 _SIGNATURES = {
     "cpattn_plan": [_P, _I32, _I32, _I32, _P, _P],
+    "cpattn_plan_2d": [_P, _I32, _I32, _I32, _P],
     "cpattn_plan_destroy": [_P],
+    "cpattn_plan_get_a2a_map": [_P, _P, _I64],
     "cpattn_plan_get_info": [_P, _P],
     "cpattn_plan_get_chunk_offsets": [_P, _P, _I64],
     "cpattn_plan_get_chunk_ranks": [_P, _P, _I64],
@@ -169,6 +171,10 @@ class Plan:
     def index_map(self):
         return self._get("cpattn_plan_get_index_map", int(self.cu_seqlens[-1]), np.int64)
 
+    def a2a_map(self):
+        """ULYSSES2D plans: the all-to-all row gather map [u*T]."""
+        return self._get("cpattn_plan_get_a2a_map", self.info()["split_h"] * int(self.cu_seqlens[-1]), np.int64)
+
     def ring_schedule(self, causal: bool):
         n = self.cp * self.cp
         kv = np.empty(n, dtype=np.int32)
@@ -185,6 +191,14 @@ def cpattn_plan(cu_seqlens, cp_size: int, mode="zigzag", grid=None) -> Plan:
     _check(lib().cpattn_plan(cu.ctypes.data, len(cu) - 1, int(cp_size), m,
                              ctypes.byref(g) if g is not None else None, ctypes.byref(h)))
     return Plan(h.value, cu, int(cp_size), m, grid)
+
+
+def cpattn_plan_2d(cu_seqlens, ulysses: int, ring: int) -> Plan:
+    """2D-Attention mesh of ulysses x ring virtual ranks (mode ulysses2d)."""
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    h = ctypes.c_void_p()
+    _check(lib().cpattn_plan_2d(cu.ctypes.data, len(cu) - 1, int(ulysses), int(ring), ctypes.byref(h)))
+    return Plan(h.value, cu, int(ulysses) * int(ring), MODES["ulysses2d"], (int(ulysses), int(ring)))
 
 
 # ------------------------------------------------------------------ attention

@@ -37,7 +37,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 struct WsLayout {
-  size_t tiles = 0, runs = 0, idx = 0, q = 0, k = 0, v = 0, total = 0;
+  size_t tiles = 0, runs = 0, idx = 0, q = 0, k = 0, v = 0, o = 0, lse = 0, total = 0;
 };
 
 size_t elem_size(cpattn_dtype_t dt) { return dt == CPATTN_DTYPE_BF16 ? 2 : 4; }
@@ -50,15 +50,22 @@ WsLayout ws_layout(const cpattn_plan_t& p, const WorkList& wl, int H, int Hkv, i
   off += align256(wl.tiles.size() * sizeof(QTile));
   L.runs = off;
   off += align256(wl.runs.size() * sizeof(KvRun));
-  if (p.mode == CPATTN_MODE_GRID2D) {
+  if (p.mode == CPATTN_MODE_GRID2D || p.mode == CPATTN_MODE_ULYSSES2D) {
+    const bool mesh = (p.mode == CPATTN_MODE_ULYSSES2D);
     L.idx = off;
-    off += align256((size_t)p.T * sizeof(int64_t));
+    off += align256((size_t)p.T * (mesh ? p.split_h : 1) * sizeof(int64_t));
     L.q = off;
     off += align256((size_t)p.T * H * D * es);
     L.k = off;
     off += align256((size_t)p.T * Hkv * D * es);
     L.v = off;
     off += align256((size_t)p.T * Hkv * D * es);
+    if (mesh) {  // head-sharded O and LSE before the reverse all-to-all
+      L.o = off;
+      off += align256((size_t)p.T * H * D * es);
+      L.lse = off;
+      off += align256((size_t)p.T * H * sizeof(float));
+    }
   }
   L.total = off;
   return L;
@@ -144,7 +151,9 @@ cpattn_status_t upload_index_map(const cpattn_plan_t* plan, uint8_t* dst, cudaSt
   {
     std::lock_guard<std::mutex> lock(g_extras_mu);
     Pinned& slot = g_extras[plan].index_map;
-    cpattn_status_t s = pinned_copy(plan->index_map.data(), plan->index_map.size() * sizeof(int64_t), &slot);
+    // GRID2D: the index map; ULYSSES2D: the all-to-all gather map
+    const std::vector<int64_t>& m = plan->mode == CPATTN_MODE_ULYSSES2D ? plan->a2a_map : plan->index_map;
+    cpattn_status_t s = pinned_copy(m.data(), m.size() * sizeof(int64_t), &slot);
     if (s != CPATTN_OK) return s;
     pm = slot;
   }
@@ -174,6 +183,12 @@ cpattn_status_t prepare(const cpattn_plan_t* plan, const void* q, const void* k,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return fail(CPATTN_INVALID_ARG, "q, k, v must be 16-byte aligned");
   if (causal && plan->mode == CPATTN_MODE_GRID2D)
     return fail(CPATTN_UNSUPPORTED, "causal masks are not defined for grid2d plans");
+  if (plan->mode == CPATTN_MODE_ULYSSES2D) {
+    if (H % plan->split_h != 0 || Hkv % plan->split_h != 0)
+      return fail(CPATTN_UNSUPPORTED, "the Ulysses degree must divide H and Hkv");
+    if ((int64_t)plan->T * plan->split_h >= (int64_t(1) << 31))
+      return fail(CPATTN_UNSUPPORTED, "u*T must be below 2^31");
+  }
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return fail(CPATTN_WORKSPACE, "workspace must be a 256-byte aligned device pointer");
   (void)ws_bytes;
   return CPATTN_OK;
@@ -253,8 +268,35 @@ cpattn_status_t cpattn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int3
     g[2] = grid->width;
   }
   std::string err;
+  if (mode == CPATTN_MODE_ULYSSES2D) {
+    delete p;
+    return fail(CPATTN_INVALID_ARG, "ulysses2d plans are made by cpattn_plan_2d");
+  }
   try {
     err = cpattn::build_plan(cu_seqlens_host, n_seqs, cp_size, (int32_t)mode, grid ? g : nullptr, p);
+  } catch (const std::exception& ex) {
+    err = std::string("planner failed: ") + ex.what();
+  }
+  if (!err.empty()) {
+    delete p;
+    return fail(CPATTN_INVALID_ARG, err);
+  }
+  *out_plan = p;
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_plan_2d(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t ulysses, int32_t ring,
+                               cpattn_plan_t** out_plan) {
+  if (!out_plan) return fail(CPATTN_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  if (ulysses < 1 || ring < 1 || (int64_t)ulysses * ring > 4096)
+    return fail(CPATTN_INVALID_ARG, "ulysses and ring must be >= 1 with ulysses*ring <= 4096");
+  auto* p = new (std::nothrow) cpattn_plan_t();
+  if (!p) return fail(CPATTN_INVALID_ARG, "out of host memory");
+  const int32_t g[3] = {ulysses, ring, 0};
+  std::string err;
+  try {
+    err = cpattn::build_plan(cu_seqlens_host, n_seqs, ulysses * ring, CPATTN_MODE_ULYSSES2D, g, p);
   } catch (const std::exception& ex) {
     err = std::string("planner failed: ") + ex.what();
   }
@@ -320,6 +362,11 @@ cpattn_status_t cpattn_plan_get_index_map(const cpattn_plan_t* plan, int64_t* ou
   CPATTN_COPY_OUT(plan->index_map);
 }
 
+cpattn_status_t cpattn_plan_get_a2a_map(const cpattn_plan_t* plan, int64_t* out, int64_t n) {
+  if (plan && plan->mode != CPATTN_MODE_ULYSSES2D) return fail(CPATTN_INVALID_ARG, "not a ulysses2d plan");
+  CPATTN_COPY_OUT(plan->a2a_map);
+}
+
 cpattn_status_t cpattn_plan_get_local_cu_seqlens(const cpattn_plan_t* plan, int32_t rank, int32_t* out, int64_t n) {
   if (!plan || !out) return fail(CPATTN_INVALID_ARG, "NULL argument");
   if (rank < 0 || rank >= plan->cp) return fail(CPATTN_INVALID_ARG, "rank out of range");
@@ -366,6 +413,9 @@ static cpattn_status_t run_attention(const cpattn_plan_t* cplan, const void* q, 
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CPATTN_INVALID_ARG, "scale must be positive and finite");
   cpattn_plan_t* plan = const_cast<cpattn_plan_t*>(cplan);
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const bool mesh = (plan->mode == CPATTN_MODE_ULYSSES2D);
+  if (mesh && q_rank >= 0)
+    return fail(CPATTN_UNSUPPORTED, "ulysses2d plans run the whole forward only (cpattn_fwd)");
   int tm, tn;
   bool pair;
   tile_sizes(dtype, &tm, &tn, &pair);
@@ -404,6 +454,37 @@ static cpattn_status_t run_attention(const cpattn_plan_t* cplan, const void* q, 
   } else {
     a.partial = true;
     a.lse_ld = plan->rank_offsets[q_rank + 1] - plan->rank_offsets[q_rank];
+  }
+  if (mesh) {
+    // the all-to-all: rows of (token, head group) gathered into head-sharded buffers
+    const int u = plan->split_h;
+    const int64_t Hs = H / u, Hks = Hkv / u, R = (int64_t)u * plan->T;
+    uint8_t* idx = ws + L_all.idx;
+    s = upload_index_map(plan, idx, stream);
+    if (s != CPATTN_OK) return s;
+    const int64_t* a2a = reinterpret_cast<const int64_t*>(idx);
+    cudaError_t e = cpattn::launch_permute_rows(q, ws + L_all.q, a2a, R, Hs * D * es, R, false, stream);
+    if (e == cudaSuccess) e = cpattn::launch_permute_rows(k, ws + L_all.k, a2a, R, Hks * D * es, R, false, stream);
+    if (e == cudaSuccess) e = cpattn::launch_permute_rows(v, ws + L_all.v, a2a, R, Hks * D * es, R, false, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "all-to-all gather");
+    a.q = ws + L_all.q;
+    a.k = ws + L_all.k;
+    a.v = ws + L_all.v;
+    a.q_rows_total = a.kv_rows_total = R;
+    a.H = (int32_t)Hs;
+    a.Hkv = (int32_t)Hks;
+    a.o = ws + L_all.o;
+    a.lse = reinterpret_cast<float*>(ws + L_all.lse);
+    a.lse_ld = R;
+    s = launch_attention(a, dtype);
+    if (s != CPATTN_OK) return s;
+    // the reverse all-to-all of O and LSE
+    e = cpattn::launch_permute_rows(ws + L_all.o, o, a2a, R, Hs * D * es, R, true, stream);
+    if (e == cudaSuccess)
+      e = cpattn::launch_lse_regroup(reinterpret_cast<const float*>(ws + L_all.lse), lse, a2a, (int)Hs, u, plan->T,
+                                     stream);
+    if (e != cudaSuccess) return cuda_fail(e, "all-to-all scatter");
+    return CPATTN_OK;
   }
   if (plan->mode == CPATTN_MODE_GRID2D) {
     // split_cp_2d: gather every rank's shard into contiguous rows
@@ -452,6 +533,7 @@ cpattn_status_t cpattn_bwd_workspace_size(const cpattn_plan_t* plan, int32_t H, 
   if (s != CPATTN_OK) return s;
   if (causal && plan->mode == CPATTN_MODE_GRID2D)
     return fail(CPATTN_UNSUPPORTED, "causal masks are not defined for grid2d plans");
+  if (plan->mode == CPATTN_MODE_ULYSSES2D) return fail(CPATTN_UNSUPPORTED, "no backward for ulysses2d plans");
   int tk, tq;
   bwd_tile_sizes(dtype, &tk, &tq);
   auto wl = cpattn::get_worklist_bwd(*const_cast<cpattn_plan_t*>(plan), causal != 0, tk, tq, -1, 0);
@@ -467,6 +549,7 @@ static cpattn_status_t run_backward(const cpattn_plan_t* cplan, const void* q, c
   cpattn_status_t s = prepare(cplan, q, k, v, dtype, H, Hkv, D, causal, workspace, ws_bytes);
   if (s == CPATTN_OK) s = check_bwd_shape(D, dtype);
   if (s != CPATTN_OK) return s;
+  if (cplan->mode == CPATTN_MODE_ULYSSES2D) return fail(CPATTN_UNSUPPORTED, "no backward for ulysses2d plans");
   if (!o || !lse || !dout) return fail(CPATTN_INVALID_ARG, "o, lse and dout must be device pointers");
   if (!dq || !dk || !dv) return fail(CPATTN_INVALID_ARG, "dq, dk and dv must be device pointers");
   if (!aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))

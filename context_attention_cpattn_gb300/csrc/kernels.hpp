@@ -108,6 +108,11 @@ cudaError_t launch_loss_norm(const float* loss, const uint8_t* valid, int64_t T,
 cudaError_t launch_permute_rows(const void* src, void* dst, const int64_t* index, int64_t rows,
                                 int64_t row_bytes, int64_t other_rows, bool scatter, cudaStream_t stream);
 
+// dst[(i*Hs + h)*T + t] = src[h*(u*T) + R] with a2a[R] = t*u + i (the reverse
+// all-to-all of a head-sharded LSE buffer).
+cudaError_t launch_lse_regroup(const float* src, float* dst, const int64_t* a2a, int Hs, int u, int64_t T,
+                               cudaStream_t stream);
+
 int num_sms();
 
 // TMA tensor maps of a [rows, heads, D] tensor viewed as (D, heads, rows):

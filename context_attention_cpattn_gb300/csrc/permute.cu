@@ -25,7 +25,31 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const uint4* __restri
   }
 }
 
+// Reverse all-to-all of the log-sum-exp: the head-sharded buffer holds
+// [H/u heads][u*T rows] (row R = i*T + p of head group i); the output is
+// [H][T] at global rows.  a2a[R] = t*u + i names the token and head group.
+__global__ void __launch_bounds__(256) lse_regroup_kernel(const float* __restrict__ src, float* __restrict__ dst,
+                                                          const int64_t* __restrict__ a2a, int Hs, int u, int64_t T) {
+  const int64_t n = (int64_t)Hs * u * T;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += stride) {
+    const int64_t hl = idx / (u * T), R = idx - hl * (u * T);
+    const int64_t m = a2a[R];
+    const int64_t t = m / u, i = m - t * u;
+    dst[(i * Hs + hl) * T + t] = src[idx];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_lse_regroup(const float* src, float* dst, const int64_t* a2a, int Hs, int u, int64_t T,
+                               cudaStream_t stream) {
+  const int64_t n = (int64_t)Hs * u * T;
+  if (n == 0) return cudaSuccess;
+  const int64_t want = (n + 255) / 256, cap = (int64_t)num_sms() * 16;
+  lse_regroup_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, stream>>>(src, dst, a2a, Hs, u, T);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_permute_rows(const void* src, void* dst, const int64_t* index, int64_t rows, int64_t row_bytes,
                                 int64_t other_rows, bool scatter, cudaStream_t stream) {

@@ -9,6 +9,10 @@
 //   strategy, get_optimal_split).
 // CONTIGUOUS: even contiguous token ranges (token stage of LongVILA MM-SP,
 //   "Scaling video training with parallelism", section 3, Fig. 2).
+// ULYSSES2D: LongVILA's 2D-Attention mesh of u Ulysses (all-to-all) x r ring
+//   (P2P) ranks (news article, 2D attention parallelism, Fig. 3 left): zigzag
+//   over the ring dimension, each ring shard's rows cut into u contiguous
+//   pieces; the all-to-all regroups them by head.
 #include "plan.hpp"
 
 #include <algorithm>
@@ -148,6 +152,84 @@ std::string build_plan(const int32_t* cu, int32_t n_seqs, int32_t cp, int32_t mo
       start = end;
     }
     p->chunk_offsets.push_back(p->T);
+  } else if (mode == CPATTN_MODE_ULYSSES2D) {
+    if (!grid) return "ulysses2d needs the mesh";
+    const int32_t u = grid[0], r = grid[1];
+    if (u < 1 || r < 1 || (int64_t)u * r != cp) return "cp must equal ulysses * ring";
+    const int C = 2 * r;
+    // ring shards: zigzag over r, local order chunk j then chunk C-1-j of each sequence
+    std::vector<std::vector<Segment>> ring(r);
+    for (int s = 0; s < n_seqs; ++s) {
+      const int64_t L = (int64_t)cu[s + 1] - cu[s];
+      if (L < C) return "ulysses2d needs every sequence to have at least 2*ring tokens";
+      const int64_t base = L / C, rem = L % C;
+      std::vector<int64_t> start(C + 1);
+      start[0] = cu[s];
+      for (int j = 0; j < C; ++j) start[j + 1] = start[j] + base + (j < rem ? 1 : 0);
+      for (int j = 0; j < r; ++j) {
+        ring[j].push_back({start[j], start[j + 1] - start[j], s, start[j] - cu[s]});
+        ring[j].push_back({start[C - 1 - j], start[C - j] - start[C - 1 - j], s, start[C - 1 - j] - cu[s]});
+      }
+    }
+    // the u Ulysses ranks of ring group j hold u contiguous pieces of its local rows
+    for (int j = 0; j < r; ++j) {
+      int64_t Tj = 0;
+      for (const Segment& sg : ring[j]) Tj += sg.len;
+      if (Tj < u) return "a ring shard has fewer tokens than the Ulysses degree";
+      const int64_t q = Tj / u, rem = Tj % u;
+      size_t si = 0;
+      int64_t used = 0;  // rows of ring[j][si] already handed out
+      for (int i = 0; i < u; ++i) {
+        int64_t need = q + (i < rem ? 1 : 0);
+        auto& dst = p->rank_segments[(size_t)j * u + i];
+        while (need > 0) {
+          const Segment& sg = ring[j][si];
+          const int64_t take = std::min(need, sg.len - used);
+          dst.push_back({sg.row0 + used, take, sg.seq, sg.pos0 + used});
+          used += take;
+          need -= take;
+          if (used == sg.len) {
+            ++si;
+            used = 0;
+          }
+        }
+      }
+    }
+    p->split_h = u;
+    p->split_w = r;
+    finish_common(p);
+    // chunks: maximal runs of consecutive global rows of one sequence owned by one rank
+    std::vector<int32_t> owner(p->T);
+    for (int g = 0; g < cp; ++g)
+      for (const Segment& sg : p->rank_segments[g])
+        for (int64_t t = 0; t < sg.len; ++t) owner[sg.row0 + t] = g;
+    int s = 0;
+    for (int64_t t = 0; t < p->T; ++t) {
+      bool new_seq = false;
+      while (cu[s + 1] <= t) {
+        ++s;
+        new_seq = true;
+      }
+      if (t == 0 || owner[t] != owner[t - 1] || new_seq) {
+        p->chunk_offsets.push_back(t);
+        p->chunk_ranks.push_back(owner[t]);
+      }
+    }
+    p->chunk_offsets.push_back(p->T);
+    // after the all-to-all: ring shard j is rows [rank_offsets[j*u], rank_offsets[(j+1)*u]) of
+    // each head group's buffer, in its zigzag local order
+    p->ring_segments.assign(r, {});
+    for (int j = 0; j < r; ++j) {
+      int64_t row = p->rank_offsets[(size_t)j * u];
+      for (const Segment& sg : ring[j]) {
+        p->ring_segments[j].push_back({row, sg.len, sg.seq, sg.pos0});
+        row += sg.len;
+      }
+    }
+    p->a2a_map.resize((size_t)u * p->T);
+    for (int i = 0; i < u; ++i)
+      for (int64_t q = 0; q < p->T; ++q) p->a2a_map[(size_t)i * p->T + q] = p->index_map[q] * u + i;
+    return std::string();
   } else {
     return "unknown mode";
   }
@@ -156,6 +238,19 @@ std::string build_plan(const int32_t* cu, int32_t n_seqs, int32_t cp, int32_t mo
 }
 
 bool ring_entry(const cpattn_plan_t& p, int r, int t, bool causal, int32_t* kv_rank, int32_t* kind) {
+  if (p.mode == CPATTN_MODE_ULYSSES2D) {
+    // after the all-to-all, rank (i, j) rings over the r ring groups with its head group
+    const int u = p.split_h, nr = p.split_w, i = r % u, j = r / u;
+    if (t >= nr) {
+      *kv_rank = -1;
+      *kind = CPATTN_MASK_SKIP;
+      return true;
+    }
+    const int k = ((j - t) % nr + nr) % nr;
+    *kv_rank = k * u + i;
+    *kind = !causal ? CPATTN_MASK_FULL : (k == j ? CPATTN_MASK_DIAG : (k < j ? CPATTN_MASK_KV_HEAD : CPATTN_MASK_Q_TAIL));
+    return true;
+  }
   const int cp = p.cp;
   const int k = ((r - t) % cp + cp) % cp;
   *kv_rank = k;
@@ -185,11 +280,15 @@ static std::pair<size_t, size_t> seq_range(const std::vector<Segment>& segs, int
 static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool causal, int tile_m,
                                                 int tile_n, bool pair, int q_rank, int step) {
   auto wl = std::make_shared<WorkList>();
-  const int cp = p.cp;
+  const bool mesh = (p.mode == CPATTN_MODE_ULYSSES2D);
+  const int cp = mesh ? p.split_w : p.cp;
   const bool gathered = (p.mode == CPATTN_MODE_GRID2D);
   // For GRID2D the kernel reads gathered shards: rank r's rows are the
   // contiguous range [rank_offsets[r], rank_offsets[r+1]) of the gathered buffers.
+  // For ULYSSES2D it reads the head-sharded buffers of the all-to-all, whose
+  // ring shards are p.ring_segments.
   auto segments_of = [&](int r) {
+    if (mesh) return p.ring_segments[r];
     if (!gathered) return p.rank_segments[r];
     std::vector<Segment> one;
     const int64_t a = p.rank_offsets[r], b = p.rank_offsets[r + 1];
@@ -248,6 +347,28 @@ static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool cau
       }
       local += qs.len;
     }
+  }
+  if (mesh) {
+    // one copy of the ring work per head group; group i's buffer rows start at i*T
+    const size_t nt = wl->tiles.size(), nr = wl->runs.size();
+    const int u = p.split_h;
+    for (int i = 1; i < u; ++i) {
+      const int32_t off = (int32_t)(i * p.T);
+      for (size_t t = 0; t < nt; ++t) {
+        QTile c = wl->tiles[t];
+        c.q_row0 += off;
+        c.out_row0 += off;
+        c.run_begin += (int32_t)(i * nr);
+        c.run_end += (int32_t)(i * nr);
+        wl->tiles.push_back(c);
+      }
+      for (size_t q = 0; q < nr; ++q) {
+        KvRun c = wl->runs[q];
+        c.kv_row0 += off;
+        wl->runs.push_back(c);
+      }
+    }
+    wl->total_kv_tiles *= u;
   }
   // Longest tiles first, so that the block scheduler's in-order dispatch
   // finishes the heaviest work early (LPT order).

@@ -52,6 +52,10 @@ struct cpattn_plan {
   std::vector<int32_t> local_cu;           // [cp*(n+1)]
   std::vector<int64_t> index_map;          // [T]
   std::vector<std::vector<cpattn::Segment>> rank_segments;  // per rank, local order
+  // ULYSSES2D: the r ring shards after the all-to-all, as segments of the
+  // head-sharded buffer (rows in index-map order), and the all-to-all gather map.
+  std::vector<std::vector<cpattn::Segment>> ring_segments;
+  std::vector<int64_t> a2a_map;            // [u*T]
 
   std::mutex mu;
   std::map<cpattn::WorkKey, std::shared_ptr<const cpattn::WorkList>> cache;

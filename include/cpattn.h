@@ -68,7 +68,8 @@ typedef enum cpattn_status {
 typedef enum cpattn_mode {
   CPATTN_MODE_ZIGZAG = 0,      /* 2*cp chunks per sequence, rank r owns r and 2cp-1-r */
   CPATTN_MODE_GRID2D = 1,      /* one F x h x w latent cut into split_h x split_w tiles */
-  CPATTN_MODE_CONTIGUOUS = 2   /* packed T cut into cp contiguous ranges              */
+  CPATTN_MODE_CONTIGUOUS = 2,  /* packed T cut into cp contiguous ranges              */
+  CPATTN_MODE_ULYSSES2D = 3    /* u x r mesh: Ulysses all-to-all x zigzag ring (cpattn_plan_2d) */
 } cpattn_mode_t;
 
 typedef enum cpattn_dtype {
@@ -98,8 +99,8 @@ typedef struct cpattn_plan_info {
   int32_t n_seqs;
   int32_t cp_size;
   int32_t mode;             /* cpattn_mode_t                                     */
-  int32_t split_h;          /* GRID2D only, else 0                               */
-  int32_t split_w;          /* GRID2D only, else 0                               */
+  int32_t split_h;          /* GRID2D: tiles per column; ULYSSES2D: u; else 0    */
+  int32_t split_w;          /* GRID2D: tiles per row; ULYSSES2D: r; else 0       */
   int32_t reserved;
 } cpattn_plan_info_t;
 
@@ -127,6 +128,26 @@ typedef struct cpattn_plan_info {
 cpattn_status_t cpattn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t cp_size,
                             cpattn_mode_t mode, const cpattn_grid_t* grid,
                             cpattn_plan_t** out_plan);
+
+/* The 2D-Attention mesh of ulysses x ring virtual ranks (LongVILA news
+ * article, 2D attention parallelism and Fig. 3 left: independent Ulysses
+ * all-to-all groups and Ring P2P groups, e.g. 8-way SP as a 4 x 2 mesh; USP
+ * and LoongTrain: "Scaling video training with parallelism", section 2).
+ * Mode CPATTN_MODE_ULYSSES2D, cp = ulysses * ring, rank g = j*ulysses + i
+ * (i: position in its Ulysses group, j: ring index).
+ *   Sequence-sharded layout (before the all-to-all): ring shard j is the
+ *   zigzag split over `ring` (chunks j and 2*ring-1-j of every sequence, each
+ *   sequence at least 2*ring tokens); its local rows are cut into `ulysses`
+ *   contiguous pieces of floor(T_j/u) + [i < T_j mod u] rows, piece i going to
+ *   rank (i, j).  rank_offsets / index_map / local_cu_seqlens describe this
+ *   layout; chunks are the maximal runs of consecutive global rows of one
+ *   sequence owned by one rank.
+ *   After the all-to-all (cpattn_plan_get_a2a_map) rank (i, j) holds every row
+ *   of ring shard j for query heads [i*H/u, (i+1)*H/u) and KV heads
+ *   [i*Hkv/u, (i+1)*Hkv/u); the ring then runs over the r ring groups.
+ * Errors: as cpattn_plan; ulysses, ring >= 1. */
+cpattn_status_t cpattn_plan_2d(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t ulysses, int32_t ring,
+                               cpattn_plan_t** out_plan);
 
 /* Free a plan (NULL is a no-op). */
 cpattn_status_t cpattn_plan_destroy(cpattn_plan_t* plan);
@@ -158,11 +179,21 @@ cpattn_status_t cpattn_plan_get_index_map(const cpattn_plan_t* plan, int64_t* ou
 cpattn_status_t cpattn_plan_get_ring_schedule(const cpattn_plan_t* plan, int32_t causal,
                                               int32_t* kv_rank, int32_t* mask_kind, int64_t n);
 
+/* ULYSSES2D plans: the all-to-all as one row gather.  Viewing a [T,H,D]
+ * tensor as [T*u, H/u*D] rows (row t*u + i = token t's head group i), row
+ * i*T + p of the head-sharded buffer is source row out[i*T + p] =
+ * index_map[p]*u + i: head group i's rows are the ring shards in ring order,
+ * each in its zigzag local order.  `out` is host int64 [u*T].  The ring
+ * schedule of these plans has (i, j) at step t < r working with the ring
+ * shard of rank ((j - t) mod r)*u + i, and kv rank -1 (SKIP) for t >= r.
+ * Other plans: CPATTN_INVALID_ARG. */
+cpattn_status_t cpattn_plan_get_a2a_map(const cpattn_plan_t* plan, int64_t* out, int64_t n);
+
 /* ---------------------------------------------------------------- attention */
 
 /* Bytes of device workspace that cpattn_fwd / cpattn_block_fwd need for this
  * plan and shape (work list, fault word and, for GRID2D, the gathered
- * shards). */
+ * shards; for ULYSSES2D, the all-to-all map and head-sharded buffers). */
 cpattn_status_t cpattn_workspace_size(const cpattn_plan_t* plan, int32_t H, int32_t Hkv, int32_t D,
                                       cpattn_dtype_t dtype, int32_t causal, size_t* bytes);
 
@@ -177,7 +208,13 @@ cpattn_status_t cpattn_workspace_size(const cpattn_plan_t* plan, int32_t H, int3
  *   workspace/ws_bytes: device scratch, >= cpattn_workspace_size().
  * GRID2D gathers each rank's shard into the workspace first (split_cp_2d)
  * and writes outputs back through the index map (gather_cp_2d).
- * Causal GRID2D is CPATTN_UNSUPPORTED. */
+ * Causal GRID2D is CPATTN_UNSUPPORTED.
+ * ULYSSES2D performs the all-to-all (a row gather of Q, K, V into
+ * head-sharded buffers in the workspace), runs every head group's ring over
+ * the r ring shards in one launch, then the reverse all-to-all of O and LSE;
+ * H and Hkv must be multiples of u (else CPATTN_UNSUPPORTED).
+ * cpattn_block_fwd, cpattn_bwd, cpattn_block_bwd and cpattn_fwd_static
+ * return CPATTN_UNSUPPORTED for ULYSSES2D plans. */
 cpattn_status_t cpattn_fwd(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
                            cpattn_dtype_t dtype, int32_t H, int32_t Hkv, int32_t D, float scale,
                            int32_t causal, void* o, float* lse, void* workspace, size_t ws_bytes,

@@ -22,6 +22,20 @@ Modes:
   two-stage MM-SP sharding, "Scaling video training with parallelism",
   section 3, Fig. 2).
 
+* ULYSSES2D - the 2D-Attention mesh of u x r virtual ranks (LongVILA news
+  article, 2D attention parallelism and Fig. 3 left: independent Ulysses
+  (all-to-all) and Ring (P2P) groups, e.g. 8-way SP as a 4 x 2 mesh; USP and
+  LoongTrain's head-context parallelism, "Scaling video training with
+  parallelism", section 2).  Rank g = j*u + i (i the Ulysses index inside a
+  ring group, j the ring index).  The ring dimension is the zigzag split over
+  r (ring shard j = chunks j and 2r-1-j of every sequence); the u ranks of
+  ring group j hold u contiguous pieces of ring shard j's local rows (sizes
+  floor(T_j/u) + [i < T_j mod u]).  The all-to-all gives rank (i, j) every
+  row of ring shard j for the query and KV heads of head group i (H/u and
+  Hkv/u heads; "Ulysses ... when the number of heads supports the split",
+  section 2).  Chunks are the maximal runs of consecutive global rows of one
+  sequence owned by one rank.
+
 Ring schedule: at step t, rank r computes with the KV shard of rank
 (r - t) mod cp ("Scaling video training with parallelism", section 2, Ring
 Attention: KV blocks circulate around the ring).  The mask kind records which
@@ -34,8 +48,8 @@ from dataclasses import dataclass
 
 import numpy as np
 
-ZIGZAG, GRID2D, CONTIGUOUS = 0, 1, 2
-MODES = {"zigzag": ZIGZAG, "grid2d": GRID2D, "contiguous": CONTIGUOUS}
+ZIGZAG, GRID2D, CONTIGUOUS, ULYSSES2D = 0, 1, 2, 3
+MODES = {"zigzag": ZIGZAG, "grid2d": GRID2D, "contiguous": CONTIGUOUS, "ulysses2d": ULYSSES2D}
 
 # mask kinds of a (q rank, ring step) pair
 SKIP, FULL, DIAG, KV_HEAD, Q_TAIL = 0, 1, 2, 3, 4
@@ -195,6 +209,46 @@ def contiguous(cu_seqlens, cp: int) -> Plan:
                 rank_offsets, _local_cu(index_map, rank_offsets, cu, cp), index_map)
 
 
+def ulysses2d(cu_seqlens, u: int, r: int) -> Plan:
+    cu = _check_cu(cu_seqlens)
+    if u < 1 or r < 1:
+        raise PlanError("ulysses and ring degrees must be >= 1")
+    T = cu[-1]
+    cp = u * r
+    ring = zigzag(cu, r)
+    per_rank = [None] * cp
+    for j in range(r):
+        rows = rank_rows(ring, j)
+        if len(rows) < u:
+            raise PlanError("a ring shard has fewer tokens than the Ulysses degree")
+        q, rem = divmod(len(rows), u)
+        start = 0
+        for i in range(u):
+            size = q + (1 if i < rem else 0)
+            per_rank[j * u + i] = rows[start:start + size]
+            start += size
+    index_map = np.concatenate(per_rank).astype(np.int64)
+    rank_offsets = np.zeros(cp + 1, dtype=np.int64)
+    rank_offsets[1:] = np.cumsum([len(x) for x in per_rank])
+    owner = np.empty(T, dtype=np.int64)
+    for g in range(cp):
+        owner[per_rank[g]] = g
+    seq = np.searchsorted(np.asarray(cu), np.arange(T), side="right") - 1
+    starts = [t for t in range(T) if t == 0 or owner[t] != owner[t - 1] or seq[t] != seq[t - 1]]
+    offs = np.asarray(starts + [T], dtype=np.int64)
+    return Plan(ULYSSES2D, cp, T, len(cu) - 1, offs, owner[starts].astype(np.int32), rank_offsets,
+                _local_cu(index_map, rank_offsets, cu, cp), index_map, u, r)
+
+
+def a2a_map(plan: Plan) -> np.ndarray:
+    """The all-to-all as one row gather: viewing a [T, H, D] tensor as
+    [T*u, H/u*D] rows (row t*u + i = token t's head group i), row
+    i*T + p of the head-sharded buffer is token index_map[p]'s head group i;
+    head group i's rows are the ring shards in ring order."""
+    u = plan.split_h
+    return np.concatenate([plan.index_map * u + i for i in range(u)]).astype(np.int64)
+
+
 def make_plan(cu_seqlens, cp: int, mode, grid=None) -> Plan:
     mode = MODES.get(mode, mode)
     if mode == ZIGZAG:
@@ -203,14 +257,34 @@ def make_plan(cu_seqlens, cp: int, mode, grid=None) -> Plan:
         return grid2d(cu_seqlens, cp, grid)
     if mode == CONTIGUOUS:
         return contiguous(cu_seqlens, cp)
+    if mode == ULYSSES2D:
+        u, r = int(grid[0]), int(grid[1])
+        if u * r != cp:
+            raise PlanError("cp must equal ulysses * ring")
+        return ulysses2d(cu_seqlens, u, r)
     raise PlanError("unknown mode")
 
 
 def ring_schedule(plan: Plan, causal: bool):
-    """(kv_rank [cp,cp], mask_kind [cp,cp]) for (q rank r, step t)."""
+    """(kv_rank [cp,cp], mask_kind [cp,cp]) for (q rank r, step t).  For a
+    ULYSSES2D plan the ring runs over the r ring groups after the all-to-all:
+    rank (i, j) at step t < r works with ring shard (j - t) mod r of its head
+    group, held by rank ((j - t) mod r)*u + i; steps t >= r are -1 / SKIP."""
     cp = plan.cp
     kv = np.zeros((cp, cp), dtype=np.int32)
     kind = np.zeros((cp, cp), dtype=np.int32)
+    if plan.mode == ULYSSES2D:
+        u, r = plan.split_h, plan.split_w
+        for g in range(cp):
+            i, j = g % u, g // u
+            for t in range(cp):
+                if t >= r:
+                    kv[g, t], kind[g, t] = -1, SKIP
+                    continue
+                k = (j - t) % r
+                kv[g, t] = k * u + i
+                kind[g, t] = FULL if not causal else (DIAG if k == j else (KV_HEAD if k < j else Q_TAIL))
+        return kv, kind
     for r in range(cp):
         for t in range(cp):
             k = (r - t) % cp

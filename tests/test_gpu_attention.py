@@ -148,3 +148,59 @@ def test_dynamic_cp_micro_batches_each_at_their_own_cp_size(cp):
         O, L = A.packed_attention(q, k, v, w.cu_seqlens, True, w.scale)
         U.check(o, lse, O, L, "bf16", f"dcp cp={cps}")
     assert len(sizes) > 1      # the batch really mixes CP sizes
+
+
+MESH = [
+    # cu_seqlens, H, Hkv, D, causal, ulysses, ring
+    ((0, 300, 557), 4, 2, 128, True, 2, 1),
+    ((0, 300, 557, 1200), 8, 4, 128, True, 2, 2),
+    ((0, 1000, 1290), 4, 4, 64, False, 4, 1),
+    ((0, 2048), 8, 8, 128, True, 4, 2),
+    ((0, 33, 250, 251 + 260), 8, 2, 128, True, 2, 4),
+]
+
+
+@pytest.mark.parametrize("case", MESH, ids=[f"mesh{i}" for i in range(len(MESH))])
+def test_ulysses_ring_mesh_forward(cp, case):
+    """2D-Attention mesh: all-to-all head regroup, ring over the ring
+    groups, reverse all-to-all; equals packed attention."""
+    cu, H, Hkv, D, causal, u, r = case
+    w = inputs.custom(cu, H, Hkv, D, dtype="bf16", causal=causal, mode="zigzag", cp=r)
+    (q, k, v), (qd, kd, vd) = U.device_inputs(w)
+    plan = cp.cpattn_plan_2d(cu, u, r)
+    o, lse = U.run_fwd(cp, plan, w, qd, kd, vd)
+    O, L = A.packed_attention(q, k, v, cu, causal, w.scale)
+    U.check(o, lse, O, L, "bf16", f"mesh {u}x{r}")
+
+
+def test_ulysses_ring_mesh_fp32(cp):
+    cu = (0, 100, 333)
+    w = inputs.custom(cu, 4, 2, 64, dtype="fp32", causal=True, mode="zigzag", cp=2)
+    (q, k, v), (qd, kd, vd) = U.device_inputs(w)
+    plan = cp.cpattn_plan_2d(cu, 2, 2)
+    o, lse = U.run_fwd(cp, plan, w, qd, kd, vd)
+    O, L = A.packed_attention(q, k, v, cu, True, w.scale)
+    U.check(o, lse, O, L, "fp32", "mesh fp32")
+
+
+def test_long_video_200k_as_the_4x2_mesh_full_size(cp):
+    w = inputs.workload("long_video_200k_gqa")
+    (q, k, v), (qd, kd, vd) = U.device_inputs(w)
+    plan = cp.cpattn_plan_2d(w.cu_seqlens, 4, 2)
+    o, lse = U.run_fwd(cp, plan, w, qd, kd, vd)
+    rows = U.boundary_rows(plan, 512, w.T, seed=w.seed)
+    O, L = A.attention_at_rows(q, k, v, w.cu_seqlens, rows, True, w.scale)
+    idx = torch.from_numpy(rows).cuda()
+    U.check(o[idx], lse[:, idx], O, L, "bf16", "long video 4x2 mesh")
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+
+
+def test_mesh_needs_heads_divisible_by_the_ulysses_degree(cp):
+    plan = cp.cpattn_plan_2d((0, 256), 4, 1)
+    qd = torch.zeros(256, 6, 128, dtype=torch.bfloat16, device="cuda")
+    kd = torch.zeros(256, 2, 128, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(cp.cpattn_workspace_size(plan, 6, 2, 128, torch.bfloat16, True), dtype=torch.uint8,
+                     device="cuda")
+    with pytest.raises(cp.CpattnError) as e:
+        cp.cpattn_fwd(plan, qd, kd, kd, torch.empty_like(qd), torch.empty(6, 256, device="cuda"), ws)
+    assert e.value.status == cp.UNSUPPORTED

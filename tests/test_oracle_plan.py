@@ -166,3 +166,68 @@ def test_contiguous_sizes():
     assert np.diff(plan.rank_offsets).tolist() == [3, 3, 3, 2]
     with pytest.raises(P.PlanError):
         P.contiguous((0, 2), 3)
+
+
+# ------------------------------------------------------- Ulysses x ring mesh
+
+def test_mesh_with_one_ulysses_rank_is_the_zigzag_ring():
+    for cu, r in (((0, 100, 357), 2), ((0, 64, 264, 520), 4), ((0, 9),  1)):
+        z, m = P.zigzag(cu, r), P.ulysses2d(cu, 1, r)
+        assert np.array_equal(z.index_map, m.index_map) and np.array_equal(z.rank_offsets, m.rank_offsets)
+
+
+def test_mesh_with_one_ring_group_is_a_contiguous_split():
+    for cu, u in (((0, 100, 357), 4), ((0, 777), 3)):
+        c, m = P.contiguous(cu, u), P.ulysses2d(cu, u, 1)
+        assert np.array_equal(m.index_map, np.arange(cu[-1])) and np.array_equal(c.rank_offsets, m.rank_offsets)
+
+
+def test_longvila_4x2_mesh_layout():
+    # 8-way SP over two nodes as a 4 x 2 mesh: ranks 0-3 (one node) share ring
+    # shard 0, ranks 4-7 ring shard 1; the Ulysses groups split each shard evenly
+    cu = (0, 1600)
+    m = P.ulysses2d(cu, 4, 2)
+    ring = P.zigzag(cu, 2)
+    assert np.array_equal(m.rank_offsets, [0, 200, 400, 600, 800, 1000, 1200, 1400, 1600])
+    assert np.array_equal(np.sort(m.index_map[:800]), np.sort(P.rank_rows(ring, 0)))
+    kv, kind = P.ring_schedule(m, True)
+    assert kv[5].tolist() == [5, 1, -1, -1, -1, -1, -1, -1]      # rank (i=1, j=1): its shard, then ring shard 0
+    assert kind[5, :2].tolist() == [P.DIAG, P.KV_HEAD]
+
+
+def test_a2a_map_is_the_head_regroup():
+    cu, u = (0, 50, 123), 2
+    m = P.ulysses2d(cu, u, 2)
+    a2a = P.a2a_map(m)
+    T, H, D = 123, 4, 3
+    assert np.array_equal(np.sort(a2a), np.arange(u * T))
+    x = np.arange(T * H * D).reshape(T, H, D)
+    buf = x.reshape(T * u, (H // u) * D)[a2a].reshape(u, T, H // u, D)
+    for i in range(u):
+        assert np.array_equal(buf[i], x[m.index_map][:, i * (H // u):(i + 1) * (H // u)])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_mesh_ring_reproduces_packed_attention(causal):
+    """Every rank (i, j) after the all-to-all: its head group's queries of ring
+    shard j over the ring shards in ring order, merged exactly, equal the
+    packed attention of those rows and heads."""
+    from oracle import attention as A
+    from oracle import merge as M
+    cu, u, r, H, Hkv, D = (0, 37, 130), 2, 2, 4, 2, 8
+    rng = np.random.default_rng(1)
+    q, k, v = rng.standard_normal((130, H, D)), rng.standard_normal((130, Hkv, D)), rng.standard_normal((130, Hkv, D))
+    O, L = A.packed_attention(q, k, v, cu, causal, 0.4)
+    m = P.ulysses2d(cu, u, r)
+    kv, _ = P.ring_schedule(m, causal)
+    ring_rows = [m.index_map[m.rank_offsets[j * u]:m.rank_offsets[(j + 1) * u]] for j in range(r)]
+    for g in range(u * r):
+        i, j = g % u, g // u
+        hs, ks = slice(i * H // u, (i + 1) * H // u), slice(i * Hkv // u, (i + 1) * Hkv // u)
+        parts = []
+        for t in range(r):
+            kr = kv[g, t] // u
+            parts.append(A.block_attention(q[:, hs], k[:, ks], v[:, ks], cu, ring_rows[j], ring_rows[kr], causal, 0.4))
+        Og, Lg = M.lse_merge([p_[0] for p_ in parts], [p_[1] for p_ in parts])
+        np.testing.assert_allclose(Og, O[ring_rows[j]][:, hs], atol=1e-12)
+        np.testing.assert_allclose(Lg, L[hs][:, ring_rows[j]], atol=1e-12)

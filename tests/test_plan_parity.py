@@ -58,3 +58,47 @@ def test_random_plans_match_oracle(cpattn, seed):
                 cpattn.cpattn_plan([0, F * h * w], cp, "grid2d", (F, h, w))
             continue
         _compare(cpattn, (0, F * h * w), cp, "grid2d", (F, h, w))
+
+
+def _compare_mesh(cpattn, cu, u, r):
+    ref = P.ulysses2d(cu, u, r)
+    got = cpattn.cpattn_plan_2d(cu, u, r)
+    info = got.info()
+    assert (info["mode"], info["cp_size"], info["split_h"], info["split_w"]) == (P.ULYSSES2D, u * r, u, r)
+    assert info["n_chunks"] == len(ref.chunk_ranks)
+    assert np.array_equal(got.chunk_offsets(), ref.chunk_offsets)
+    assert np.array_equal(got.chunk_ranks(), ref.chunk_ranks)
+    assert np.array_equal(got.rank_offsets(), ref.rank_offsets)
+    assert np.array_equal(got.index_map(), ref.index_map)
+    assert np.array_equal(got.a2a_map(), P.a2a_map(ref))
+    for g in range(u * r):
+        assert np.array_equal(got.local_cu_seqlens(g), ref.local_cu_seqlens[g])
+    for causal in (False, True):
+        kv, kind = got.ring_schedule(causal)
+        rkv, rkind = P.ring_schedule(ref, causal)
+        assert np.array_equal(kv, rkv) and np.array_equal(kind, rkind)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_ulysses_ring_mesh_plans_match_oracle(cpattn, seed):
+    rng = np.random.default_rng(50 + seed)
+    for u, r in ((1, 1), (1, 4), (2, 1), (2, 2), (4, 2), (3, 3), (8, 1)):
+        lens = rng.integers(2 * r, 400, size=rng.integers(1, 6))
+        cu = np.concatenate([[0], np.cumsum(lens)])
+        _compare_mesh(cpattn, cu, u, r)
+
+
+def test_long_video_as_the_4x2_mesh_matches_oracle(cpattn):
+    w = inputs.workload("long_video_200k_gqa")
+    _compare_mesh(cpattn, w.cu_seqlens, 4, 2)
+
+
+def test_mesh_plan_errors(cpattn):
+    with pytest.raises(cpattn.CpattnError):
+        cpattn.cpattn_plan_2d((0, 3), 1, 2)        # a sequence shorter than 2*ring
+    with pytest.raises(cpattn.CpattnError):
+        cpattn.cpattn_plan_2d((0, 8), 5, 2)        # ring shards of 4 tokens for 5 Ulysses ranks
+    with pytest.raises(cpattn.CpattnError):
+        cpattn.cpattn_plan((0, 64), 4, "ulysses2d")  # only cpattn_plan_2d builds mesh plans
+    with pytest.raises(cpattn.CpattnError):
+        cpattn.cpattn_plan((0, 64), 4, "zigzag").a2a_map()
