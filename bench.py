@@ -319,11 +319,15 @@ def run_ours(args, rep: Replicas):
     if args.mesh:
         u, r = (int(x) for x in args.mesh.lower().split("x"))
         plan = cp.cpattn_plan_2d(w.cu_seqlens, u, r)
+    elif w.mode == "paired":
+        plan = cp.cpattn_plan_paired(w.cu_seqlens, w.cp, w.grid[0])
     else:
         plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
     ws_bytes = cp.cpattn_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal)
     plan_ms = 1e3 * (time.perf_counter() - t0)
-    flops = cp.cpattn_fwd_flops(w.cu_seqlens, w.H, w.D, w.causal)
+    # FLOPs over the pairs the mask allows (teacher forcing for paired plans)
+    flops = (4 * w.D * w.H * plan.allowed_pairs(True) if w.mode == "paired"
+             else cp.cpattn_fwd_flops(w.cu_seqlens, w.H, w.D, w.causal))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     o = torch.empty_like(qd)
     lse = torch.empty((w.H, w.T), dtype=torch.float32, device=dev)
@@ -332,7 +336,7 @@ def run_ours(args, rep: Replicas):
     stream = torch.cuda.current_stream(dev)
     # attention + loss; grid2d adds 3 shard gathers; the mesh adds 3 all-to-all gathers,
     # the reverse all-to-all of O and the LSE regroup
-    launches_per_step = 2 + (5 if args.mesh else 3 if w.mode == "grid2d" else 0)
+    launches_per_step = 2 + (5 if args.mesh or w.mode == "paired" else 3 if w.mode == "grid2d" else 0)
 
     def step(ev0=None, ev1=None):
         if ev0 is not None:
@@ -428,7 +432,8 @@ def run_ours(args, rep: Replicas):
         "fwd_ms_min": min(fwd_ms),
         "tc_source_sha256": tc_source_hash(),
     }
-    if not args.no_cpu_baseline and rep.world == 1:
+    if not args.no_cpu_baseline and rep.world == 1 and w.mode != "paired":
+        # (the CPU legs evaluate the causal / bidirectional oracle; paired plans use another mask)
         line["cpu_baseline"] = run_cpu_baseline(args)
     print(json.dumps(line), flush=True)
 

@@ -23,7 +23,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "cpattn.h")
 
 OK, INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA_ERROR, DEVICE_FAULT = range(6)
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "CUDA_ERROR", 5: "DEVICE_FAULT"}
-MODES = {"zigzag": 0, "grid2d": 1, "contiguous": 2, "ulysses2d": 3}
+MODES = {"zigzag": 0, "grid2d": 1, "contiguous": 2, "ulysses2d": 3, "paired": 4}
 DTYPE_FP32, DTYPE_BF16 = 0, 1
 MASK_SKIP, MASK_FULL, MASK_DIAG, MASK_KV_HEAD, MASK_Q_TAIL = range(5)
 
@@ -55,6 +55,8 @@ _P, _I32, _I64, _SZ, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, cty
 _SIGNATURES = {
     "cpattn_plan": [_P, _I32, _I32, _I32, _P, _P],
     "cpattn_plan_2d": [_P, _I32, _I32, _I32, _P],
+    "cpattn_plan_paired": [_P, _I32, _I32, _I32, _P],
+    "cpattn_plan_allowed_pairs": [_P, _I32, _P],
     "cpattn_plan_destroy": [_P],
     "cpattn_plan_get_a2a_map": [_P, _P, _I64],
     "cpattn_plan_get_info": [_P, _P],
@@ -171,8 +173,13 @@ class Plan:
     def index_map(self):
         return self._get("cpattn_plan_get_index_map", int(self.cu_seqlens[-1]), np.int64)
 
+    def allowed_pairs(self, causal: bool = True) -> int:
+        out = ctypes.c_uint64()
+        _check(lib().cpattn_plan_allowed_pairs(self._h, int(bool(causal)), ctypes.byref(out)))
+        return int(out.value)
+
     def a2a_map(self):
-        """ULYSSES2D plans: the all-to-all row gather map [u*T]."""
+        """ULYSSES2D and PAIRED plans: the all-to-all row gather map [u*T]."""
         return self._get("cpattn_plan_get_a2a_map", self.info()["split_h"] * int(self.cu_seqlens[-1]), np.int64)
 
     def ring_schedule(self, causal: bool):
@@ -199,6 +206,14 @@ def cpattn_plan_2d(cu_seqlens, ulysses: int, ring: int) -> Plan:
     h = ctypes.c_void_p()
     _check(lib().cpattn_plan_2d(cu.ctypes.data, len(cu) - 1, int(ulysses), int(ring), ctypes.byref(h)))
     return Plan(h.value, cu, int(ulysses) * int(ring), MODES["ulysses2d"], (int(ulysses), int(ring)))
+
+
+def cpattn_plan_paired(cu_seqlens, cp_size: int, n_chunks: int) -> Plan:
+    """Clean/noisy time-chunk pairs for teacher forcing (mode paired)."""
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    h = ctypes.c_void_p()
+    _check(lib().cpattn_plan_paired(cu.ctypes.data, len(cu) - 1, int(cp_size), int(n_chunks), ctypes.byref(h)))
+    return Plan(h.value, cu, int(cp_size), MODES["paired"], (int(n_chunks),))
 
 
 # ------------------------------------------------------------------ attention

@@ -34,6 +34,9 @@ cpattn_status_t cuda_fail(cudaError_t e, const char* what) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Plans whose forward runs on head-sharded buffers behind a Ulysses all-to-all.
+bool head_sharded(int mode) { return mode == CPATTN_MODE_ULYSSES2D || mode == CPATTN_MODE_PAIRED; }
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 struct WsLayout {
@@ -50,8 +53,8 @@ WsLayout ws_layout(const cpattn_plan_t& p, const WorkList& wl, int H, int Hkv, i
   off += align256(wl.tiles.size() * sizeof(QTile));
   L.runs = off;
   off += align256(wl.runs.size() * sizeof(KvRun));
-  if (p.mode == CPATTN_MODE_GRID2D || p.mode == CPATTN_MODE_ULYSSES2D) {
-    const bool mesh = (p.mode == CPATTN_MODE_ULYSSES2D);
+  if (p.mode == CPATTN_MODE_GRID2D || head_sharded(p.mode)) {
+    const bool mesh = head_sharded(p.mode);
     L.idx = off;
     off += align256((size_t)p.T * (mesh ? p.split_h : 1) * sizeof(int64_t));
     L.q = off;
@@ -152,7 +155,7 @@ cpattn_status_t upload_index_map(const cpattn_plan_t* plan, uint8_t* dst, cudaSt
     std::lock_guard<std::mutex> lock(g_extras_mu);
     Pinned& slot = g_extras[plan].index_map;
     // GRID2D: the index map; ULYSSES2D: the all-to-all gather map
-    const std::vector<int64_t>& m = plan->mode == CPATTN_MODE_ULYSSES2D ? plan->a2a_map : plan->index_map;
+    const std::vector<int64_t>& m = head_sharded(plan->mode) ? plan->a2a_map : plan->index_map;
     cpattn_status_t s = pinned_copy(m.data(), m.size() * sizeof(int64_t), &slot);
     if (s != CPATTN_OK) return s;
     pm = slot;
@@ -183,7 +186,9 @@ cpattn_status_t prepare(const cpattn_plan_t* plan, const void* q, const void* k,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return fail(CPATTN_INVALID_ARG, "q, k, v must be 16-byte aligned");
   if (causal && plan->mode == CPATTN_MODE_GRID2D)
     return fail(CPATTN_UNSUPPORTED, "causal masks are not defined for grid2d plans");
-  if (plan->mode == CPATTN_MODE_ULYSSES2D) {
+  if (plan->mode == CPATTN_MODE_PAIRED && !causal)
+    return fail(CPATTN_UNSUPPORTED, "paired plans apply the teacher-forcing mask (causal must be 1)");
+  if (head_sharded(plan->mode)) {
     if (H % plan->split_h != 0 || Hkv % plan->split_h != 0)
       return fail(CPATTN_UNSUPPORTED, "the Ulysses degree must divide H and Hkv");
     if ((int64_t)plan->T * plan->split_h >= (int64_t(1) << 31))
@@ -268,9 +273,9 @@ cpattn_status_t cpattn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int3
     g[2] = grid->width;
   }
   std::string err;
-  if (mode == CPATTN_MODE_ULYSSES2D) {
+  if (head_sharded(mode)) {
     delete p;
-    return fail(CPATTN_INVALID_ARG, "ulysses2d plans are made by cpattn_plan_2d");
+    return fail(CPATTN_INVALID_ARG, "ulysses2d and paired plans are made by cpattn_plan_2d / cpattn_plan_paired");
   }
   try {
     err = cpattn::build_plan(cu_seqlens_host, n_seqs, cp_size, (int32_t)mode, grid ? g : nullptr, p);
@@ -305,6 +310,53 @@ cpattn_status_t cpattn_plan_2d(const int32_t* cu_seqlens_host, int32_t n_seqs, i
     return fail(CPATTN_INVALID_ARG, err);
   }
   *out_plan = p;
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_plan_paired(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t cp_size,
+                                   int32_t n_chunks, cpattn_plan_t** out_plan) {
+  if (!out_plan) return fail(CPATTN_INVALID_ARG, "out_plan is NULL");
+  *out_plan = nullptr;
+  if (cp_size < 1 || cp_size > 4096) return fail(CPATTN_INVALID_ARG, "cp_size must be in [1, 4096]");
+  auto* p = new (std::nothrow) cpattn_plan_t();
+  if (!p) return fail(CPATTN_INVALID_ARG, "out of host memory");
+  const int32_t g[3] = {n_chunks, 0, 0};
+  std::string err;
+  try {
+    err = cpattn::build_plan(cu_seqlens_host, n_seqs, cp_size, CPATTN_MODE_PAIRED, g, p);
+  } catch (const std::exception& ex) {
+    err = std::string("planner failed: ") + ex.what();
+  }
+  if (!err.empty()) {
+    delete p;
+    return fail(CPATTN_INVALID_ARG, err);
+  }
+  *out_plan = p;
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_plan_allowed_pairs(const cpattn_plan_t* plan, int32_t causal, uint64_t* out) {
+  if (!plan || !out) return fail(CPATTN_INVALID_ARG, "NULL argument");
+  uint64_t total = 0;
+  if (plan->mode == CPATTN_MODE_PAIRED) {
+    // clean chunk j sees clean chunks <= j; noisy chunk j sees clean chunks < j and itself
+    const int N = plan->tf_chunks;
+    for (int s = 0; s < plan->n_seqs; ++s) {
+      uint64_t prefix = 0;
+      for (int j = 0; j < N; ++j) {
+        const uint64_t c = (uint64_t)plan->tf_clean[(size_t)s * N + j].len;
+        const uint64_t n = (uint64_t)plan->tf_noisy[(size_t)s * N + j].len;
+        total += c * (prefix + c) + n * (prefix + n);
+        prefix += c;
+      }
+    }
+  } else {
+    for (int s = 0; s < plan->n_seqs; ++s) {
+      const uint64_t L = (uint64_t)(plan->cu[s + 1] - plan->cu[s]);
+      total += causal ? L * (L + 1) / 2 : L * L;
+    }
+  }
+  *out = total;
   return CPATTN_OK;
 }
 
@@ -363,7 +415,7 @@ cpattn_status_t cpattn_plan_get_index_map(const cpattn_plan_t* plan, int64_t* ou
 }
 
 cpattn_status_t cpattn_plan_get_a2a_map(const cpattn_plan_t* plan, int64_t* out, int64_t n) {
-  if (plan && plan->mode != CPATTN_MODE_ULYSSES2D) return fail(CPATTN_INVALID_ARG, "not a ulysses2d plan");
+  if (plan && !head_sharded(plan->mode)) return fail(CPATTN_INVALID_ARG, "not a ulysses2d or paired plan");
   CPATTN_COPY_OUT(plan->a2a_map);
 }
 
@@ -413,9 +465,9 @@ static cpattn_status_t run_attention(const cpattn_plan_t* cplan, const void* q, 
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CPATTN_INVALID_ARG, "scale must be positive and finite");
   cpattn_plan_t* plan = const_cast<cpattn_plan_t*>(cplan);
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  const bool mesh = (plan->mode == CPATTN_MODE_ULYSSES2D);
+  const bool mesh = head_sharded(plan->mode);
   if (mesh && q_rank >= 0)
-    return fail(CPATTN_UNSUPPORTED, "ulysses2d plans run the whole forward only (cpattn_fwd)");
+    return fail(CPATTN_UNSUPPORTED, "ulysses2d and paired plans run the whole forward only (cpattn_fwd)");
   int tm, tn;
   bool pair;
   tile_sizes(dtype, &tm, &tn, &pair);
@@ -533,7 +585,7 @@ cpattn_status_t cpattn_bwd_workspace_size(const cpattn_plan_t* plan, int32_t H, 
   if (s != CPATTN_OK) return s;
   if (causal && plan->mode == CPATTN_MODE_GRID2D)
     return fail(CPATTN_UNSUPPORTED, "causal masks are not defined for grid2d plans");
-  if (plan->mode == CPATTN_MODE_ULYSSES2D) return fail(CPATTN_UNSUPPORTED, "no backward for ulysses2d plans");
+  if (head_sharded(plan->mode)) return fail(CPATTN_UNSUPPORTED, "no backward for ulysses2d or paired plans");
   int tk, tq;
   bwd_tile_sizes(dtype, &tk, &tq);
   auto wl = cpattn::get_worklist_bwd(*const_cast<cpattn_plan_t*>(plan), causal != 0, tk, tq, -1, 0);
@@ -549,7 +601,7 @@ static cpattn_status_t run_backward(const cpattn_plan_t* cplan, const void* q, c
   cpattn_status_t s = prepare(cplan, q, k, v, dtype, H, Hkv, D, causal, workspace, ws_bytes);
   if (s == CPATTN_OK) s = check_bwd_shape(D, dtype);
   if (s != CPATTN_OK) return s;
-  if (cplan->mode == CPATTN_MODE_ULYSSES2D) return fail(CPATTN_UNSUPPORTED, "no backward for ulysses2d plans");
+  if (head_sharded(cplan->mode)) return fail(CPATTN_UNSUPPORTED, "no backward for ulysses2d or paired plans");
   if (!o || !lse || !dout) return fail(CPATTN_INVALID_ARG, "o, lse and dout must be device pointers");
   if (!dq || !dk || !dv) return fail(CPATTN_INVALID_ARG, "dq, dk and dv must be device pointers");
   if (!aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))

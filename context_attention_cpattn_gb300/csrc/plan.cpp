@@ -9,6 +9,12 @@
 //   strategy, get_optimal_split).
 // CONTIGUOUS: even contiguous token ranges (token stage of LongVILA MM-SP,
 //   "Scaling video training with parallelism", section 3, Fig. 2).
+// PAIRED: LongLive-2.0's balanced SP ("Scaling video training with
+//   parallelism", section 4): each sample is [clean ; noisy] over N time
+//   chunks, rank k keeps the clean/noisy pairs of its time chunks, and after
+//   the Ulysses all-to-all the teacher-forcing mask (clean chunk j sees clean
+//   chunks <= j; noisy chunk j sees clean chunks < j and itself) is applied
+//   at chunk granularity by the work list.
 // ULYSSES2D: LongVILA's 2D-Attention mesh of u Ulysses (all-to-all) x r ring
 //   (P2P) ranks (news article, 2D attention parallelism, Fig. 3 left): zigzag
 //   over the ring dimension, each ring shard's rows cut into u contiguous
@@ -58,6 +64,14 @@ static void finish_common(cpattn_plan_t* p) {
     int32_t* lc = &p->local_cu[(size_t)r * (n + 1)];
     for (int s = 0; s < n; ++s) lc[s + 1] = lc[s] + (int32_t)per_seq[s];
   }
+}
+
+// The Ulysses all-to-all as one row gather: head-sharded row i*T + q holds
+// source row index_map[q]*u + i of the [T*u, H/u*D] view.
+static void build_a2a(cpattn_plan_t* p, int u) {
+  p->a2a_map.resize((size_t)u * p->T);
+  for (int i = 0; i < u; ++i)
+    for (int64_t q = 0; q < p->T; ++q) p->a2a_map[(size_t)i * p->T + q] = p->index_map[q] * u + i;
 }
 
 std::string build_plan(const int32_t* cu, int32_t n_seqs, int32_t cp, int32_t mode,
@@ -226,9 +240,64 @@ std::string build_plan(const int32_t* cu, int32_t n_seqs, int32_t cp, int32_t mo
         row += sg.len;
       }
     }
-    p->a2a_map.resize((size_t)u * p->T);
-    for (int i = 0; i < u; ++i)
-      for (int64_t q = 0; q < p->T; ++q) p->a2a_map[(size_t)i * p->T + q] = p->index_map[q] * u + i;
+    build_a2a(p, u);
+    return std::string();
+  } else if (mode == CPATTN_MODE_PAIRED) {
+    if (!grid) return "paired plans need the number of time chunks";
+    const int32_t N = grid[0];
+    if (N < 1 || N % cp != 0) return "the number of time chunks must be a positive multiple of cp";
+    const int32_t m = N / cp;
+    // per sample: [clean ; noisy], each stream in N chunks of floor(half/N) + [j < half mod N] tokens
+    std::vector<int64_t> cstart((size_t)n_seqs * (N + 1)), nstart((size_t)n_seqs * (N + 1));
+    for (int s = 0; s < n_seqs; ++s) {
+      const int64_t L = (int64_t)cu[s + 1] - cu[s];
+      if (L % 2 != 0 || L / 2 < N) return "paired samples need an even length with at least N tokens per stream";
+      const int64_t half = L / 2;
+      int64_t* cs = &cstart[(size_t)s * (N + 1)];
+      int64_t* ns = &nstart[(size_t)s * (N + 1)];
+      cs[0] = cu[s];
+      ns[0] = cu[s] + half;
+      for (int j = 0; j < N; ++j) {
+        const int64_t sz = half / N + (j < half % N ? 1 : 0);
+        cs[j + 1] = cs[j] + sz;
+        ns[j + 1] = ns[j] + sz;
+      }
+      for (int j = 0; j < N; ++j) {
+        auto& dst = p->rank_segments[(size_t)(j / m)];
+        dst.push_back({cs[j], cs[j + 1] - cs[j], s, cs[j] - cu[s]});
+        dst.push_back({ns[j], ns[j + 1] - ns[j], s, ns[j] - cu[s]});
+      }
+      // chunks in global order: the clean chunks, then the noisy chunks
+      for (int j = 0; j < N; ++j) {
+        p->chunk_offsets.push_back(cs[j]);
+        p->chunk_ranks.push_back(j / m);
+      }
+      for (int j = 0; j < N; ++j) {
+        p->chunk_offsets.push_back(ns[j]);
+        p->chunk_ranks.push_back(j / m);
+      }
+    }
+    p->chunk_offsets.push_back(p->T);
+    p->split_h = cp;  // a Ulysses layout over all cp ranks with one ring group
+    p->split_w = 1;
+    finish_common(p);
+    // the clean and noisy chunks in the head-sharded buffer (rows in index-map order)
+    p->tf_chunks = N;
+    p->tf_clean.assign((size_t)n_seqs * N, {});
+    p->tf_noisy.assign((size_t)n_seqs * N, {});
+    std::vector<int64_t> row(cp);
+    for (int k = 0; k < cp; ++k) row[k] = p->rank_offsets[k];
+    for (int s = 0; s < n_seqs; ++s)
+      for (int j = 0; j < N; ++j) {
+        const int64_t* cs = &cstart[(size_t)s * (N + 1)];
+        const int64_t* ns = &nstart[(size_t)s * (N + 1)];
+        int64_t& r = row[j / m];
+        p->tf_clean[(size_t)s * N + j] = {r, cs[j + 1] - cs[j], s, cs[j] - cu[s]};
+        r += cs[j + 1] - cs[j];
+        p->tf_noisy[(size_t)s * N + j] = {r, ns[j + 1] - ns[j], s, ns[j] - cu[s]};
+        r += ns[j + 1] - ns[j];
+      }
+    build_a2a(p, cp);
     return std::string();
   } else {
     return "unknown mode";
@@ -238,8 +307,9 @@ std::string build_plan(const int32_t* cu, int32_t n_seqs, int32_t cp, int32_t mo
 }
 
 bool ring_entry(const cpattn_plan_t& p, int r, int t, bool causal, int32_t* kv_rank, int32_t* kind) {
-  if (p.mode == CPATTN_MODE_ULYSSES2D) {
+  if (p.mode == CPATTN_MODE_ULYSSES2D || p.mode == CPATTN_MODE_PAIRED) {
     // after the all-to-all, rank (i, j) rings over the r ring groups with its head group
+    // (PAIRED: one ring group, every key local after the all-to-all)
     const int u = p.split_h, nr = p.split_w, i = r % u, j = r / u;
     if (t >= nr) {
       *kv_rank = -1;
@@ -277,10 +347,73 @@ static std::pair<size_t, size_t> seq_range(const std::vector<Segment>& segs, int
   return {(size_t)(lo - segs.begin()), (size_t)(hi - segs.begin())};
 }
 
+// Replicates a work list over the u head groups of a head-sharded buffer
+// (group i's rows start at i*T).
+static void replicate_head_groups(const cpattn_plan_t& p, WorkList* wl) {
+  const size_t nt = wl->tiles.size(), nr = wl->runs.size();
+  const int u = p.split_h;
+  for (int i = 1; i < u; ++i) {
+    const int32_t off = (int32_t)(i * p.T);
+    for (size_t t = 0; t < nt; ++t) {
+      QTile c = wl->tiles[t];
+      c.q_row0 += off;
+      c.out_row0 += off;
+      c.run_begin += (int32_t)(i * nr);
+      c.run_end += (int32_t)(i * nr);
+      wl->tiles.push_back(c);
+    }
+    for (size_t q = 0; q < nr; ++q) {
+      KvRun c = wl->runs[q];
+      c.kv_row0 += off;
+      wl->runs.push_back(c);
+    }
+  }
+  wl->total_kv_tiles *= u;
+}
+
+// PAIRED: the teacher-forcing mask at chunk granularity; every run is fully visible.
+static std::shared_ptr<WorkList> build_worklist_paired(const cpattn_plan_t& p, int tile_m, int tile_n, bool pair) {
+  auto wl = std::make_shared<WorkList>();
+  const int N = p.tf_chunks;
+  for (int s = 0; s < p.n_seqs; ++s)
+    for (int j = 0; j < N; ++j)
+      for (int noisy = 0; noisy < 2; ++noisy) {
+        const Segment& qs = noisy ? p.tf_noisy[(size_t)s * N + j] : p.tf_clean[(size_t)s * N + j];
+        std::vector<Segment> keys;
+        for (int jj = 0; jj < (noisy ? j : j + 1); ++jj) keys.push_back(p.tf_clean[(size_t)s * N + jj]);
+        if (noisy) keys.push_back(qs);
+        for (int64_t off = 0; off < qs.len; off += tile_m) {
+          QTile t{};
+          const int64_t rows = std::min<int64_t>(tile_m, qs.len - off);
+          t.q_row0 = (int32_t)(qs.row0 + off);
+          t.q_pos0 = (int32_t)(qs.pos0 + off);
+          t.q_rows = (int32_t)rows;
+          t.out_row0 = t.q_row0;
+          t.rank = j / (N / p.cp);
+          t.run_begin = (int32_t)wl->runs.size();
+          int64_t ntiles = 0;
+          for (const Segment& ks : keys) {
+            wl->runs.push_back({(int32_t)ks.row0, (int32_t)ks.pos0, (int32_t)ks.len, 0});
+            ntiles += (ks.len + tile_n - 1) / tile_n;
+          }
+          t.run_end = (int32_t)wl->runs.size();
+          if (pair) ntiles = (ntiles + 1) / 2;
+          t.n_kv_tiles = (int32_t)ntiles;
+          wl->total_kv_tiles += ntiles;
+          wl->tiles.push_back(t);
+        }
+      }
+  replicate_head_groups(p, wl.get());
+  std::stable_sort(wl->tiles.begin(), wl->tiles.end(),
+                   [](const QTile& a, const QTile& b) { return a.n_kv_tiles > b.n_kv_tiles; });
+  return wl;
+}
+
 static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool causal, int tile_m,
                                                 int tile_n, bool pair, int q_rank, int step) {
+  if (p.mode == CPATTN_MODE_PAIRED) return build_worklist_paired(p, tile_m, tile_n, pair);
   auto wl = std::make_shared<WorkList>();
-  const bool mesh = (p.mode == CPATTN_MODE_ULYSSES2D);
+  const bool mesh = (p.mode == CPATTN_MODE_ULYSSES2D);  // (PAIRED returned above)
   const int cp = mesh ? p.split_w : p.cp;
   const bool gathered = (p.mode == CPATTN_MODE_GRID2D);
   // For GRID2D the kernel reads gathered shards: rank r's rows are the
@@ -348,28 +481,7 @@ static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool cau
       local += qs.len;
     }
   }
-  if (mesh) {
-    // one copy of the ring work per head group; group i's buffer rows start at i*T
-    const size_t nt = wl->tiles.size(), nr = wl->runs.size();
-    const int u = p.split_h;
-    for (int i = 1; i < u; ++i) {
-      const int32_t off = (int32_t)(i * p.T);
-      for (size_t t = 0; t < nt; ++t) {
-        QTile c = wl->tiles[t];
-        c.q_row0 += off;
-        c.out_row0 += off;
-        c.run_begin += (int32_t)(i * nr);
-        c.run_end += (int32_t)(i * nr);
-        wl->tiles.push_back(c);
-      }
-      for (size_t q = 0; q < nr; ++q) {
-        KvRun c = wl->runs[q];
-        c.kv_row0 += off;
-        wl->runs.push_back(c);
-      }
-    }
-    wl->total_kv_tiles *= u;
-  }
+  if (mesh) replicate_head_groups(p, wl.get());  // one copy of the ring work per head group
   // Longest tiles first, so that the block scheduler's in-order dispatch
   // finishes the heaviest work early (LPT order).
   std::stable_sort(wl->tiles.begin(), wl->tiles.end(),

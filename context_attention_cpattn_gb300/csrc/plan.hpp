@@ -56,6 +56,10 @@ struct cpattn_plan {
   // head-sharded buffer (rows in index-map order), and the all-to-all gather map.
   std::vector<std::vector<cpattn::Segment>> ring_segments;
   std::vector<int64_t> a2a_map;            // [u*T]
+  // PAIRED: per sample s and time chunk j (index s*tf_chunks + j), the clean
+  // and the noisy chunk as segments of the head-sharded buffer.
+  int32_t tf_chunks = 0;
+  std::vector<cpattn::Segment> tf_clean, tf_noisy;
 
   std::mutex mu;
   std::map<cpattn::WorkKey, std::shared_ptr<const cpattn::WorkList>> cache;

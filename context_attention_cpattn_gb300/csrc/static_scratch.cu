@@ -74,10 +74,11 @@ extern "C" cpattn_status_t cpattn_fwd_static(const cpattn_plan_t* cplan, const v
                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
   if (mis & 15) return set_error(CPATTN_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
   if (!(scale > 0.f) || !std::isfinite(scale)) return set_error(CPATTN_INVALID_ARG, "scale must be positive and finite");
-  if (cplan->mode == CPATTN_MODE_GRID2D || cplan->mode == CPATTN_MODE_ULYSSES2D)
+  if (cplan->mode == CPATTN_MODE_GRID2D || cplan->mode == CPATTN_MODE_ULYSSES2D ||
+      cplan->mode == CPATTN_MODE_PAIRED)
     return set_error(CPATTN_UNSUPPORTED,
-                     "cpattn_fwd_static has no room to gather grid2d or ulysses2d shards; use cpattn_fwd with a "
-                     "workspace");
+                     "cpattn_fwd_static has no room to gather grid2d, ulysses2d or paired shards; use cpattn_fwd "
+                     "with a workspace");
 
   cpattn_plan_t* plan = const_cast<cpattn_plan_t*>(cplan);
   const bool bf16 = dtype == CPATTN_DTYPE_BF16;

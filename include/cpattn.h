@@ -69,7 +69,8 @@ typedef enum cpattn_mode {
   CPATTN_MODE_ZIGZAG = 0,      /* 2*cp chunks per sequence, rank r owns r and 2cp-1-r */
   CPATTN_MODE_GRID2D = 1,      /* one F x h x w latent cut into split_h x split_w tiles */
   CPATTN_MODE_CONTIGUOUS = 2,  /* packed T cut into cp contiguous ranges              */
-  CPATTN_MODE_ULYSSES2D = 3    /* u x r mesh: Ulysses all-to-all x zigzag ring (cpattn_plan_2d) */
+  CPATTN_MODE_ULYSSES2D = 3,   /* u x r mesh: Ulysses all-to-all x zigzag ring (cpattn_plan_2d) */
+  CPATTN_MODE_PAIRED = 4       /* clean/noisy time-chunk pairs, teacher forcing (cpattn_plan_paired) */
 } cpattn_mode_t;
 
 typedef enum cpattn_dtype {
@@ -99,8 +100,8 @@ typedef struct cpattn_plan_info {
   int32_t n_seqs;
   int32_t cp_size;
   int32_t mode;             /* cpattn_mode_t                                     */
-  int32_t split_h;          /* GRID2D: tiles per column; ULYSSES2D: u; else 0    */
-  int32_t split_w;          /* GRID2D: tiles per row; ULYSSES2D: r; else 0       */
+  int32_t split_h;          /* GRID2D: tiles per column; ULYSSES2D: u; PAIRED: cp; else 0 */
+  int32_t split_w;          /* GRID2D: tiles per row; ULYSSES2D: r; PAIRED: 1; else 0     */
   int32_t reserved;
 } cpattn_plan_info_t;
 
@@ -149,6 +150,28 @@ cpattn_status_t cpattn_plan(const int32_t* cu_seqlens_host, int32_t n_seqs, int3
 cpattn_status_t cpattn_plan_2d(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t ulysses, int32_t ring,
                                cpattn_plan_t** out_plan);
 
+/* LongLive-2.0's balanced SP for autoregressive teacher forcing ("Scaling
+ * video training with parallelism", section 4): each sample of L tokens (L
+ * even) is [clean history ; noisy target], each stream cut into n_chunks time
+ * chunks of floor((L/2)/N) + [j < (L/2) mod N] tokens (at least one each).
+ * Rank k keeps time chunks [k*m, (k+1)*m) (m = n_chunks / cp_size, which must
+ * be an integer), each as its clean chunk then its noisy chunk; the forward
+ * runs behind a Ulysses all-to-all over all cp ranks (split_h = cp, split_w =
+ * 1, cpattn_plan_get_a2a_map) with the teacher-forcing mask in that order:
+ * a clean token of chunk j sees the clean tokens of chunks <= j, a noisy token
+ * of chunk j the clean tokens of chunks < j and the noisy tokens of chunk j
+ * (the page is cut off before it states the mask; this is the reading used).
+ * Chunks are listed clean chunks first, then noisy chunks, per sample.
+ * cpattn_fwd needs causal = 1 (the teacher-forcing mask) and H, Hkv multiples
+ * of cp.  Errors: as cpattn_plan. */
+cpattn_status_t cpattn_plan_paired(const int32_t* cu_seqlens_host, int32_t n_seqs, int32_t cp_size,
+                                   int32_t n_chunks, cpattn_plan_t** out_plan);
+
+/* Number of (query, key) pairs that a plan's mask allows: per sequence
+ * L(L+1)/2 (causal) or L^2, or the teacher-forcing count of a PAIRED plan.
+ * Forward FLOPs = 4 * D * H * pairs. */
+cpattn_status_t cpattn_plan_allowed_pairs(const cpattn_plan_t* plan, int32_t causal, uint64_t* out);
+
 /* Free a plan (NULL is a no-op). */
 cpattn_status_t cpattn_plan_destroy(cpattn_plan_t* plan);
 
@@ -179,7 +202,7 @@ cpattn_status_t cpattn_plan_get_index_map(const cpattn_plan_t* plan, int64_t* ou
 cpattn_status_t cpattn_plan_get_ring_schedule(const cpattn_plan_t* plan, int32_t causal,
                                               int32_t* kv_rank, int32_t* mask_kind, int64_t n);
 
-/* ULYSSES2D plans: the all-to-all as one row gather.  Viewing a [T,H,D]
+/* ULYSSES2D and PAIRED plans: the all-to-all as one row gather.  Viewing a [T,H,D]
  * tensor as [T*u, H/u*D] rows (row t*u + i = token t's head group i), row
  * i*T + p of the head-sharded buffer is source row out[i*T + p] =
  * index_map[p]*u + i: head group i's rows are the ring shards in ring order,
@@ -213,8 +236,9 @@ cpattn_status_t cpattn_workspace_size(const cpattn_plan_t* plan, int32_t H, int3
  * head-sharded buffers in the workspace), runs every head group's ring over
  * the r ring shards in one launch, then the reverse all-to-all of O and LSE;
  * H and Hkv must be multiples of u (else CPATTN_UNSUPPORTED).
+ * PAIRED plans take the same path with the teacher-forcing mask (causal = 1).
  * cpattn_block_fwd, cpattn_bwd, cpattn_block_bwd and cpattn_fwd_static
- * return CPATTN_UNSUPPORTED for ULYSSES2D plans. */
+ * return CPATTN_UNSUPPORTED for ULYSSES2D and PAIRED plans. */
 cpattn_status_t cpattn_fwd(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
                            cpattn_dtype_t dtype, int32_t H, int32_t Hkv, int32_t D, float scale,
                            int32_t causal, void* o, float* lse, void* workspace, size_t ws_bytes,

@@ -156,6 +156,11 @@ def workload(name: str, seed: int = DEFAULT_SEED) -> Workload:
         return Workload(name, (0, 1 << 20), H=32, Hkv=8, D=128, dtype="bf16",
                         causal=True, mode="zigzag", cp=16,
                         value_scale=1.0 / math.sqrt(128), seed=seed)
+    if name == "teacher_forcing_pairs":
+        # [clean ; noisy] x 8 time chunks of 3 latent frames x (30 x 52) patches; grid = (time chunks,)
+        return Workload(name, (0, 2 * 8 * 3 * 30 * 52), H=24, Hkv=24, D=128, dtype="bf16",
+                        causal=True, mode="paired", cp=8, grid=(8,),
+                        value_scale=1.0 / math.sqrt(128), seed=seed)
     raise KeyError(name)
 
 

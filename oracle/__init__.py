@@ -31,14 +31,19 @@ Contents and the passages each follows:
 * ``loss`` - per-token loss normalisation over valid tokens (Dynamic-CP
   article, section "Loss computation and FLOPS statistics").
 * ``flops`` - THD-aware FLOP count from real sequence lengths (same section).
+* ``teacher_forcing`` - LongLive-2.0's clean/noisy pairs: the teacher-forcing
+  mask, dense masked attention, the paired plan ("Scaling video training with
+  parallelism", section 4).  The mask is a reading of a truncated page:
+  parity partly unpinned.
 * ``dcp`` - the Dynamic-CP scheduler: Eq. 1-3 quotas, per-sample CP size,
   packing into micro-batches and the micro-batch count sweep (Dynamic-CP
   article, data-scheduling and runtime sections).
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against brute
-force, closed forms, library routines and invariants.  One exception is
-partial: ``dcp.schedule`` follows a prose heuristic, so past its invariants,
-bounds and a hand-worked case its parity is unpinned.
+force, closed forms, library routines and invariants.  Two are partial:
+``dcp.schedule`` follows a prose heuristic and ``teacher_forcing.allowed`` a
+mask the page does not finish stating, so past their pins their parity is
+unpinned.
 """
 
-from . import attention, attention_bwd, dcp, flops, loss, merge, plan  # noqa: F401
+from . import attention, attention_bwd, dcp, flops, loss, merge, plan, teacher_forcing  # noqa: F401

@@ -48,7 +48,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-ZIGZAG, GRID2D, CONTIGUOUS, ULYSSES2D = 0, 1, 2, 3
+ZIGZAG, GRID2D, CONTIGUOUS, ULYSSES2D, PAIRED = 0, 1, 2, 3, 4
 MODES = {"zigzag": ZIGZAG, "grid2d": GRID2D, "contiguous": CONTIGUOUS, "ulysses2d": ULYSSES2D}
 
 # mask kinds of a (q rank, ring step) pair
@@ -273,7 +273,7 @@ def ring_schedule(plan: Plan, causal: bool):
     cp = plan.cp
     kv = np.zeros((cp, cp), dtype=np.int32)
     kind = np.zeros((cp, cp), dtype=np.int32)
-    if plan.mode == ULYSSES2D:
+    if plan.mode in (ULYSSES2D, PAIRED):   # PAIRED: a Ulysses layout with one ring group
         u, r = plan.split_h, plan.split_w
         for g in range(cp):
             i, j = g % u, g // u

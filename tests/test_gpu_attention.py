@@ -204,3 +204,60 @@ def test_mesh_needs_heads_divisible_by_the_ulysses_degree(cp):
     with pytest.raises(cp.CpattnError) as e:
         cp.cpattn_fwd(plan, qd, kd, kd, torch.empty_like(qd), torch.empty(6, 256, device="cuda"), ws)
     assert e.value.status == cp.UNSUPPORTED
+
+
+PAIRED = [
+    # cu_seqlens, H, Hkv, D, cp, time chunks
+    ((0, 40, 100), 4, 2, 128, 2, 4),
+    ((0, 512), 8, 8, 128, 4, 8),
+    ((0, 300, 700), 8, 4, 64, 2, 2),
+    ((0, 2 * 4 * 300), 4, 4, 128, 4, 4),
+]
+
+
+@pytest.mark.parametrize("case", PAIRED, ids=[f"paired{i}" for i in range(len(PAIRED))])
+def test_paired_teacher_forcing_forward(cp, case):
+    """Clean/noisy pairs behind the Ulysses all-to-all with the
+    teacher-forcing mask; equals the dense-mask oracle."""
+    from oracle import teacher_forcing as TF
+    cu, H, Hkv, D, cps, N = case
+    w = inputs.custom(cu, H, Hkv, D, dtype="bf16", causal=True, mode="zigzag", cp=1)
+    (q, k, v), (qd, kd, vd) = U.device_inputs(w)
+    plan = cp.cpattn_plan_paired(cu, cps, N)
+    o, lse = U.run_fwd(cp, plan, w, qd, kd, vd)
+    O, L = TF.masked_attention(q, k, v, TF.allowed(cu, N), w.scale)
+    U.check(o, lse, O, L, "bf16", f"paired cp={cps} N={N}")
+
+
+def test_paired_teacher_forcing_fp32(cp):
+    from oracle import teacher_forcing as TF
+    cu = (0, 64, 200)
+    w = inputs.custom(cu, 4, 2, 64, dtype="fp32", causal=True, mode="zigzag", cp=1)
+    (q, k, v), (qd, kd, vd) = U.device_inputs(w)
+    plan = cp.cpattn_plan_paired(cu, 2, 4)
+    o, lse = U.run_fwd(cp, plan, w, qd, kd, vd)
+    O, L = TF.masked_attention(q, k, v, TF.allowed(cu, 4), w.scale)
+    U.check(o, lse, O, L, "fp32", "paired fp32")
+
+
+def test_teacher_forcing_pairs_full_size(cp):
+    from oracle import teacher_forcing as TF
+    w = inputs.workload("teacher_forcing_pairs")
+    (q, k, v), (qd, kd, vd) = U.device_inputs(w)
+    plan = cp.cpattn_plan_paired(w.cu_seqlens, w.cp, w.grid[0])
+    o, lse = U.run_fwd(cp, plan, w, qd, kd, vd)
+    rows = U.boundary_rows(plan, 384, w.T, seed=w.seed)
+    O, L = TF.attention_at_rows(q, k, v, w.cu_seqlens, w.grid[0], rows, w.scale)
+    idx = torch.from_numpy(rows).cuda()
+    U.check(o[idx], lse[:, idx], O, L, "bf16", "teacher forcing pairs")
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+
+
+def test_paired_plans_need_the_teacher_forcing_mask(cp):
+    plan = cp.cpattn_plan_paired((0, 256), 2, 2)
+    qd = torch.zeros(256, 2, 128, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(cp.cpattn_workspace_size(plan, 2, 2, 128, torch.bfloat16, False), dtype=torch.uint8,
+                     device="cuda")
+    with pytest.raises(cp.CpattnError) as e:
+        cp.cpattn_fwd(plan, qd, qd, qd, torch.empty_like(qd), torch.empty(2, 256, device="cuda"), ws, causal=False)
+    assert e.value.status == cp.UNSUPPORTED

@@ -102,3 +102,38 @@ def test_mesh_plan_errors(cpattn):
         cpattn.cpattn_plan((0, 64), 4, "ulysses2d")  # only cpattn_plan_2d builds mesh plans
     with pytest.raises(cpattn.CpattnError):
         cpattn.cpattn_plan((0, 64), 4, "zigzag").a2a_map()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_paired_plans_match_oracle(cpattn, seed):
+    from oracle import teacher_forcing as TF
+    rng = np.random.default_rng(80 + seed)
+    for cp in (1, 2, 4):
+        N = cp * int(rng.integers(1, 4))
+        lens = 2 * rng.integers(N, 200, size=rng.integers(1, 4))
+        cu = np.concatenate([[0], np.cumsum(lens)])
+        ref = TF.paired_plan(cu, cp, N)
+        got = cpattn.cpattn_plan_paired(cu, cp, N)
+        info = got.info()
+        assert (info["mode"], info["split_h"], info["split_w"]) == (TF.PAIRED, cp, 1)
+        assert np.array_equal(got.chunk_offsets(), ref.chunk_offsets)
+        assert np.array_equal(got.chunk_ranks(), ref.chunk_ranks)
+        assert np.array_equal(got.rank_offsets(), ref.rank_offsets)
+        assert np.array_equal(got.index_map(), ref.index_map)
+        assert np.array_equal(got.a2a_map(), P.a2a_map(ref))
+        for r in range(cp):
+            assert np.array_equal(got.local_cu_seqlens(r), ref.local_cu_seqlens[r])
+        kv, kind = got.ring_schedule(True)
+        rkv, rkind = P.ring_schedule(ref, True)
+        assert np.array_equal(kv, rkv) and np.array_equal(kind, rkind)
+        assert got.allowed_pairs() == TF.allowed_pairs(cu, N)
+    with pytest.raises(cpattn.CpattnError):
+        cpattn.cpattn_plan_paired((0, 41), 1, 2)       # odd length
+    with pytest.raises(cpattn.CpattnError):
+        cpattn.cpattn_plan_paired((0, 40), 3, 4)       # chunks not a multiple of cp
+
+
+def test_allowed_pairs_of_standard_plans(cpattn):
+    cu = (0, 10, 30)
+    pl = cpattn.cpattn_plan(cu, 2, "zigzag")
+    assert pl.allowed_pairs(True) == 55 + 210 and pl.allowed_pairs(False) == 100 + 400
