@@ -9,12 +9,12 @@
 // ring step's partial (O_t, lse_t) is folded in as soon as it is produced and
 // never leaves the SM.
 //
-// Persistent blocks, two per SM (about 99 KB of shared memory and 256 TMEM
+// Persistent blocks, two per SM (about 101 KB of shared memory and 256 TMEM
 // columns each).  The producer warp hands out work items (the first by block
 // index, the rest from an atomic counter, longest first) through a ring of
 // shared-memory slots.
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer: Q per item, then K_j and V_j through two-deep
 //               rings; K_j is refilled once S_j has read it, V_j once PV_j has.
 //   warp 1      TMEM allocator and MMA issuer (one thread).  TMEM holds two S
@@ -26,12 +26,17 @@
 //               warps work on this one.  P_j is written over the first 32
 //               columns of S_j's buffer; S_{j+2} reuses that buffer after PV_j
 //               (tcgen05.mma ops from one thread run in issue order).
-//   warps 2-5   softmax + epilogue, one query row per thread: read S_j from
-//               TMEM, apply the causal / run-end mask from token positions,
-//               update the running max and sum, write P (bf16 pairs) back to
-//               TMEM, and rescale O when the running max grows by more than
-//               2^8 (otherwise the stale max is kept: O and the sum share it,
-//               so the final O/l is exact).  A rescale first waits for PV_{j-1}.
+//   warps 2-5   softmax, one query row per thread: read S_j from TMEM, apply
+//               the causal / run-end mask from token positions, update the
+//               running max and sum, write P (bf16 pairs) back to TMEM, and
+//               rescale O when the running max grows by more than 2^8
+//               (otherwise the stale max is kept: O and the sum share it, so
+//               the final O/l is exact).  A rescale first waits for PV_{j-1}.
+//               At the end of an item the row's max and sum go to shared
+//               memory and the warps move on to the next item at once.
+//   warps 6-9   epilogue, one query row per thread: once the item's last PV
+//               has run, read O from TMEM, release it for the next item's
+//               first PV, and write O/l and the LSE at the output rows.
 //
 // Shared-memory operand layouts (1024-byte aligned, SWIZZLE_128B):
 //   Q:    [128 rows][64 columns] boxes, K-major.
@@ -79,8 +84,9 @@ struct TcCfg {
   static constexpr uint32_t OFF_K = Q_BYTES;          // K[2]
   static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;  // V[2]
   static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // 26 mbarriers (208 bytes) fit below
-  static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // 27 mbarriers (216 bytes) fit below
+  static constexpr uint32_t OFF_STATS = OFF_MISC + 64;  // [2 items][128 rows] (max, sum)
+  static constexpr uint32_t SMEM = OFF_STATS + 2 * 128 * 8 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 256;              // S0 | S1 | O
   static constexpr uint32_t TM_S = 0, TM_O = 128;         // S buffer b at TM_S + 64 b
 };
@@ -124,7 +130,7 @@ __device__ __forceinline__ Item item_of(int i, int n_tiles, int G) {
 }
 
 template <int D, bool kPartial>
-__global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<D>;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
@@ -147,10 +153,12 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
   uint64_t* drain = bars + 17;
   uint64_t* item_full = bars + 18;   // [4] ring of work items handed from the producer
   uint64_t* item_empty = bars + 22;  // [4]
+  uint64_t* stats_full = bars + 26;  // the softmax warps have left an item's row max and sum
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);     // loads issued: [0] K, [1] V, [2] Q
   int* item_ring = reinterpret_cast<int*>(smem + C::OFF_MISC + 32);  // [4]
+  float2* stats = reinterpret_cast<float2*>(smem + C::OFF_STATS);     // [2][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.H / p.Hkv;
@@ -171,9 +179,10 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
     mbar_init(o_final, 1);
     mbar_init(o_free, 128);
     mbar_init(drain, 1);
+    mbar_init(stats_full, 128);
     for (int r = 0; r < 4; ++r) {
       mbar_init(item_full + r, 1);
-      mbar_init(item_empty + r, 129);  // the MMA thread and the 128 softmax threads
+      mbar_init(item_empty + r, 257);  // the MMA thread, 128 softmax and 128 epilogue threads
     }
     *abort_flag = 0;
     issued[0] = issued[1] = issued[2] = 0;
@@ -309,8 +318,8 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
       umma_commit(drain);
       drain_wait(drain, 0);
     }
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ softmax
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
@@ -406,14 +415,36 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
         mbar_arrive(p_full + b);
       }
       if (!ok) break;
-
       if (n_kv > 0) {
-        if (!__all_sync(0xffffffffu, wait_bounded(o_final, oc & 1, abort_flag, p.ws, 15))) break;
-        tc_fence_after();
+        // the row's running max and sum for the epilogue warps
+        stats[(oc & 1) * 128 + row] = make_float2(m_ref, l);
+        mbar_arrive(stats_full);
+        ++oc;
       }
-      // epilogue: O / l and LSE at the output rows
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+    int oc = 0;
+    for (int k = 0;; ++k) {
+      const int i = take_item(k, 16);
+      if (!__all_sync(0xffffffffu, i != -2)) break;
+      if (i < 0) break;
       const Item it = item_of(i, p.n_tiles, G);
       const QTile tile = p.tiles[it.tile_id];
+      const int n_kv = tile.n_kv_tiles;
+      float m_raw = -INFINITY, l = 0.f;
+      if (n_kv > 0) {
+        if (!__all_sync(0xffffffffu, wait_bounded(o_final, oc & 1, abort_flag, p.ws, 15) &&
+                                         wait_bounded(stats_full, oc & 1, abort_flag, p.ws, 17)))
+          break;
+        tc_fence_after();
+        const float2 st = stats[(oc & 1) * 128 + row];
+        m_raw = st.x;
+        l = st.y;
+      }
       const bool valid_row = row < tile.q_rows;
       const bool has = l > 0.f;
       const float inv_l = has ? 1.f / l : 0.f;
@@ -424,6 +455,11 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
         uint32_t o[32];
         if (n_kv > 0) {
           tmem_ld32_wait(tl + C::TM_O + 32u * cb, o);
+          if (cb == D / 32 - 1) {
+            // O has been read: the next item's first PV may overwrite it
+            tc_fence_before();
+            mbar_arrive(o_free);
+          }
         } else {
 #pragma unroll
           for (int q = 0; q < 32; ++q) o[q] = 0u;
@@ -446,13 +482,8 @@ __global__ void __launch_bounds__(192, 2) attn_fwd_tc_kernel(const __grid_consta
           }
         }
       }
-      if (valid_row) p.lse[(int64_t)it.h * p.lse_ld + out_row] = has ? m_ref * p.scale + logf(l) : -INFINITY;
-      if (n_kv > 0) {
-        // O has been read: the next item's first PV may overwrite it
-        tc_fence_before();
-        mbar_arrive(o_free);
-        ++oc;
-      }
+      if (valid_row) p.lse[(int64_t)it.h * p.lse_ld + out_row] = has ? m_raw * p.scale + logf(l) : -INFINITY;
+      if (n_kv > 0) ++oc;
     }
   }
 
@@ -483,7 +514,7 @@ static cudaError_t launch_tc(const TcParams& p, int n_blocks, cudaStream_t strea
   const uint32_t smem = TcCfg<D>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<n_blocks, 192, smem, stream>>>(p);
+  kern<<<n_blocks, 320, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
