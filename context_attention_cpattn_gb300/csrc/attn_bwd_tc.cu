@@ -598,33 +598,44 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
 }
 
 // delta = rowsum(dO * O), -lse * log2(e) and (optionally) a zeroed dQ
-// accumulator row, one warp per (buffer row, head).  Rows of O, dO and LSE
-// are read at in_map[row] when a map is given (buffers of gathered shards).
-template <typename T>
+// accumulator row.  A group of D*sizeof(T)/16 lanes (16-byte loads) per
+// (buffer row, head); rows of O, dO and LSE are read at in_map[row] when a map
+// is given (buffers of gathered shards).
+template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dout,
                                                       const float* __restrict__ lse, int64_t lse_ld,
-                                                      const int64_t* __restrict__ in_map, int64_t rows, int H, int D,
+                                                      const int64_t* __restrict__ in_map, int64_t rows, int H,
                                                       float* __restrict__ nl2, float* __restrict__ nd,
                                                       float* __restrict__ dq_zero) {
-  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= rows * H) return;
-  const int64_t row = wid / H;
-  const int h = (int)(wid % H);
-  const int64_t src = in_map ? in_map[row] : row;
-  const T* orow = o + (src * H + h) * D;
-  const T* drow = dout + (src * H + h) * D;
+  constexpr int kPer = 16 / sizeof(T);  // elements per 16-byte load
+  constexpr int kLanes = D / kPer;      // lanes per (row, head): 8 or 16 (bf16), 16 or 32 (fp32)
+  const int64_t gid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / kLanes;
+  const int sub = threadIdx.x % kLanes;
+  const bool active = gid < rows * H;
+  const int64_t row = active ? gid / H : 0;
+  const int h = active ? (int)(gid % H) : 0;
+  const int64_t src = active ? (in_map ? in_map[row] : row) : 0;
   float acc = 0.f;
-  for (int c = lane; c < D; c += 32) acc += (float)orow[c] * (float)drow[c];
+  if (active) {
+    const uint4 a = reinterpret_cast<const uint4*>(o + (src * H + h) * D)[sub];
+    const uint4 b = reinterpret_cast<const uint4*>(dout + (src * H + h) * D)[sub];
+    const T* av = reinterpret_cast<const T*>(&a);
+    const T* bv = reinterpret_cast<const T*>(&b);
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
+    for (int e = 0; e < kPer; ++e) acc += (float)av[e] * (float)bv[e];
+  }
+#pragma unroll
+  for (int s = kLanes / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (!active) return;
+  if (sub == 0) {
     const float l = lse[(int64_t)h * lse_ld + src];
     nl2[(int64_t)h * rows + row] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
     nd[(int64_t)h * rows + row] = -acc;
   }
-  if (dq_zero)
-    for (int c = lane; c < D; c += 32) dq_zero[(row * H + h) * D + c] = 0.f;
+  if (dq_zero) {
+    float4* z = reinterpret_cast<float4*>(dq_zero + (row * H + h) * D);
+    for (int c = sub; c < D / 4; c += kLanes) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 // From the fp32 dQ accumulator (buffer rows) to the output: row r goes to
@@ -665,18 +676,21 @@ cudaError_t launch_bwd_tc(const BwdParams& p, int n_blocks, cudaStream_t stream)
 
 }  // namespace
 
+template <typename T, int D>
+static void pre_launch(const BwdArgs& a) {
+  constexpr int kLanes = D / (16 / sizeof(T));
+  const int64_t threads = a.rows_total * a.H * kLanes;
+  bwd_pre_kernel<T, D><<<(unsigned)((threads + 255) / 256), 256, 0, a.stream>>>(
+      static_cast<const T*>(a.o), static_cast<const T*>(a.dout), a.lse, a.lse_ld, a.in_map, a.rows_total, a.H,
+      a.nl2, a.nd, a.zero_dq ? a.dq_acc : nullptr);
+}
+
 cudaError_t launch_bwd_pre(const BwdArgs& a) {
-  const int64_t warps = a.rows_total * a.H;
-  if (warps == 0) return cudaSuccess;
-  const int64_t blocks = (warps * 32 + 255) / 256;
+  if (a.rows_total * a.H == 0) return cudaSuccess;
   if (a.bf16)
-    bwd_pre_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, a.stream>>>(
-        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.lse_ld, a.in_map,
-        a.rows_total, a.H, a.D, a.nl2, a.nd, a.zero_dq ? a.dq_acc : nullptr);
+    a.D == 128 ? pre_launch<__nv_bfloat16, 128>(a) : pre_launch<__nv_bfloat16, 64>(a);
   else
-    bwd_pre_kernel<float><<<(unsigned)blocks, 256, 0, a.stream>>>(
-        static_cast<const float*>(a.o), static_cast<const float*>(a.dout), a.lse, a.lse_ld, a.in_map, a.rows_total,
-        a.H, a.D, a.nl2, a.nd, a.zero_dq ? a.dq_acc : nullptr);
+    a.D == 128 ? pre_launch<float, 128>(a) : pre_launch<float, 64>(a);
   return cudaGetLastError();
 }
 
