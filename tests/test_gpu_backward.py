@@ -149,8 +149,9 @@ def test_dynamic_cp_microbatch_backward_full_size(cp):
     """The 32K-token micro-batch (H = 32, D = 128, zigzag cp = 4): dQ at every
     chunk-boundary row plus 512 sampled rows from the oracle row by row; dK and
     dV of every sequence of at most 2048 tokens from the full oracle; and on
-    every sequence and KV head the invariants sum_j dV_j = sum_i dO_i and
-    sum_j dK_j = 0 (relative to the summed magnitudes)."""
+    every sequence and KV head the invariants sum_j dV_j = sum_i dO_i
+    (relative to sqrt(sum_i |dO_i|^2)) and sum_j dK_j = 0 (relative to
+    sqrt(sum_j |dK_j|^2))."""
     w = inputs.workload("dynamic_cp_microbatch")
     (q, k, v, do), (qd, kd, vd, dod), plan, o, lse = _setup(cp, w)
     dq, dk, dv = _run_bwd(cp, plan, w, qd, kd, vd, o, lse, dod)
@@ -178,8 +179,70 @@ def test_dynamic_cp_microbatch_backward_full_size(cp):
             heads = [h for h in range(w.H) if h * w.Hkv // w.H == g]
             lhs = dv64[a:b, g].sum(axis=0)
             rhs = do64[a:b][:, heads].sum(axis=(0, 1))
-            worst_v = max(worst_v, np.linalg.norm(lhs - rhs) / np.sqrt((dv64[a:b, g] ** 2).sum() + 1e-30))
+            worst_v = max(worst_v, np.linalg.norm(lhs - rhs) / np.sqrt((do64[a:b][:, heads] ** 2).sum() + 1e-30))
             worst_k = max(worst_k, np.linalg.norm(dk64[a:b, g].sum(axis=0)) /
                           np.sqrt((dk64[a:b, g] ** 2).sum() + 1e-30))
     print("invariants: sum dV - sum dO", worst_v, "sum dK", worst_k)
     assert worst_v <= 2e-2 and worst_k <= 2e-2
+
+
+@pytest.mark.parametrize("dtype,mode", [("bf16", "contiguous"), ("fp32", "contiguous")])
+def test_block_backward_contiguous_ring(cp, dtype, mode):
+    cu = (0, 700, 1500, 1501, 2600) if dtype == "bf16" else (0, 90, 200, 201, 300)
+    w = inputs.custom(cu, 8, 2, 128 if dtype == "bf16" else 64, dtype=dtype, causal=True, mode=mode, cp=3)
+    (q, k, v, do), (qd, kd, vd, dod), plan, o, lse = _setup(cp, w)
+    T, H, D = qd.shape
+    ws = torch.empty(cp.cpattn_bwd_workspace_size(plan, H, 2, D, qd.dtype, True), dtype=torch.uint8, device="cuda")
+    acc = [torch.zeros(T, n, D, dtype=torch.float32, device="cuda") for n in (H, 2, 2)]
+    for r in range(w.cp):
+        for t in range(w.cp):
+            cp.cpattn_block_bwd(plan, qd, kd, vd, o, lse, dod, *acc, ws, r, t, scale=w.scale, causal=True)
+            cp.cpattn_sync_status(ws)
+    check_grads(acc, B.packed_attention_bwd(q, k, v, do, cu, True, w.scale), dtype, f"ring {dtype} {mode}")
+
+
+def test_bf16_backward_gqa_group_of_eight(cp):
+    cu = (0, 700, 1500)
+    w = inputs.custom(cu, 32, 4, 128, dtype="bf16", causal=True, mode="zigzag", cp=2)
+    (q, k, v, do), (qd, kd, vd, dod), plan, o, lse = _setup(cp, w)
+    got = _run_bwd(cp, plan, w, qd, kd, vd, o, lse, dod)
+    check_grads(got, B.packed_attention_bwd(q, k, v, do, cu, True, w.scale), "bf16", "gqa 32/4")
+
+
+def _full_size_single_sequence(cp, name, n_rows):
+    """One long sequence at full size: dQ at chunk-boundary and sampled rows
+    from the oracle row by row, and sum_j dV_j = sum_i dO_i, sum_j dK_j = 0 on
+    every KV head.  The dV bound is relative to sqrt(sum_i |dO_i|^2): with
+    near-uniform attention every P of a row sits near 1/row, so its bf16
+    rounding carries a per-row bias of up to 2^-9 that the sum over rows
+    weights by dO_i; the dK bound is relative to sqrt(sum_j |dK_j|^2)."""
+    w = inputs.workload(name)
+    (q, k, v, do), (qd, kd, vd, dod), plan, o, lse = _setup(cp, w)
+    dq, dk, dv = _run_bwd(cp, plan, w, qd, kd, vd, o, lse, dod)
+    rows = inputs.sample_rows(w.T, n_rows, w.seed, must_include=plan.chunk_offsets()[1:-1][:64].tolist())
+    ref = B.dq_at_rows(q, k, v, do, w.cu_seqlens, rows, w.causal, w.scale)
+    got = dq[torch.from_numpy(rows).cuda()].to("cpu", torch.float64).numpy()
+    err = got - ref
+    rel = np.sqrt((err ** 2).sum(axis=(0, 2))) / np.sqrt((ref ** 2).sum(axis=(0, 2)))
+    assert rel.max() <= BWD_BF16_REL_RMS, rel.max()
+    assert np.abs(err).max() <= BWD_BF16_MAX * np.abs(ref).max()
+    G = w.H // w.Hkv
+    sum_dv = dv.to(torch.float64).sum(dim=0)                    # [Hkv, D]
+    do_g = dod.to(torch.float64).view(w.T, w.Hkv, G, w.D)
+    sum_do = do_g.sum(dim=(0, 2))
+    norm_v = do_g.pow(2).sum(dim=(0, 2, 3)).sqrt()
+    worst_v = ((sum_dv - sum_do).norm(dim=1) / norm_v).max().item()
+    sum_dk = dk.to(torch.float64).sum(dim=0)
+    norm_k = dk.to(torch.float64).pow(2).sum(dim=(0, 2)).sqrt()
+    worst_k = (sum_dk.norm(dim=1) / norm_k).max().item()
+    print(name, "dQ rel rms", rel.max(), "invariants", worst_v, worst_k)
+    assert worst_v <= 2e-2 and worst_k <= 2e-2
+    assert torch.isfinite(dk).all() and torch.isfinite(dv).all() and torch.isfinite(dq).all()
+
+
+def test_long_video_200k_backward_full_size(cp):
+    _full_size_single_sequence(cp, "long_video_200k_gqa", 192)
+
+
+def test_video_latent_grid2d_backward_full_size(cp):
+    _full_size_single_sequence(cp, "video_latent_grid2d", 256)
