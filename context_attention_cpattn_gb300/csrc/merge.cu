@@ -3,10 +3,12 @@
 // Ring attention leaves one partial (O_p, lse_p) per KV block ("Scaling video
 // training with parallelism", section 2, Ring Attention); combining them
 // exactly is M = max lse_p, lse = M + ln sum exp(lse_p - M),
-// O = sum exp(lse_p - lse) O_p.  One warp per (row, head): each lane owns D/32
-// consecutive elements and reads them with one vector load per partial; the
-// per-partial weights are computed once per warp with shuffles.  The grid is a
-// multiple of the SM count and strides over (row, head) pairs.
+// O = sum exp(lse_p - lse) O_p.  One warp per (row, head), head-major so that
+// neighbouring warps read neighbouring LSE entries: lane i reads the lse of
+// partials i and i + 32 once, the weights are formed once and broadcast with
+// shuffles, and each lane owns D/32 consecutive elements, loading four
+// partials' vectors before their multiply-adds.  The grid is a multiple of the
+// SM count and strides over (head, row) pairs.
 #include <cmath>
 
 #include "common.cuh"
@@ -34,41 +36,61 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ Merg
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t total = p.rows * p.H;
+  // head-major order: neighbouring warps read neighbouring LSE entries
   for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total; w += warps) {
-    const int64_t row = w / p.H;
-    const int h = (int)(w - row * p.H);
-    // max of the partials' lse (each lane takes partials lane, lane+32)
-    float mx = -INFINITY;
-    for (int i = lane; i < p.n; i += 32) mx = fmaxf(mx, p.lse_parts[i][(int64_t)h * p.rows + row]);
+    const int h = (int)(w / p.rows);
+    const int64_t row = w - (int64_t)h * p.rows;
+    const int64_t li_off = (int64_t)h * p.rows + row;
+    // lane i holds the lse of partials i and i + 32, read once
+    const float l0 = lane < p.n ? p.lse_parts[lane][li_off] : -INFINITY;
+    const float l1 = lane + 32 < p.n ? p.lse_parts[lane + 32][li_off] : -INFINITY;
+    float mx = fmaxf(l0, l1);
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-    float z = 0.f;
-    if (mx != -INFINITY)
-      for (int i = lane; i < p.n; i += 32) z += expf(p.lse_parts[i][(int64_t)h * p.rows + row] - mx);
+    const bool has = mx != -INFINITY;
+    float z = has ? expf(l0 - mx) + expf(l1 - mx) : 0.f;
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) z += __shfl_xor_sync(0xffffffffu, z, s);
-    const bool has = mx != -INFINITY;
     const float lse = has ? mx + logf(z) : -INFINITY;
+    const float w0 = has ? expf(l0 - lse) : 0.f;  // weight of partial lane (0 for -inf)
+    const float w1 = has ? expf(l1 - lse) : 0.f;  // weight of partial lane + 32
 
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     if (has) {
-      for (int i = 0; i < p.n; ++i) {
-        const float li = p.lse_parts[i][(int64_t)h * p.rows + row];
-        if (li == -INFINITY) continue;
-        const float wgt = expf(li - lse);
-        const float* src = p.o_parts[i] + (row * p.H + h) * D + lane * E;
-        if constexpr (E == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(src);
-          acc[0] = fmaf(wgt, x.x, acc[0]);
-          acc[1] = fmaf(wgt, x.y, acc[1]);
-          acc[2] = fmaf(wgt, x.z, acc[2]);
-          acc[3] = fmaf(wgt, x.w, acc[3]);
-        } else {
-          const float2 x = *reinterpret_cast<const float2*>(src);
-          acc[0] = fmaf(wgt, x.x, acc[0]);
-          acc[1] = fmaf(wgt, x.y, acc[1]);
+      // four partials' loads in flight before their multiply-adds
+      for (int i0 = 0; i0 < p.n; i0 += 4) {
+        float x[4][E];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = i0 + k;
+          if (i < p.n) {
+            const float* src = p.o_parts[i] + (row * p.H + h) * D + lane * E;
+            if constexpr (E == 4) {
+              const float4 v = *reinterpret_cast<const float4*>(src);
+              x[k][0] = v.x;
+              x[k][1] = v.y;
+              x[k][2] = v.z;
+              x[k][3] = v.w;
+            } else {
+              const float2 v = *reinterpret_cast<const float2*>(src);
+              x[k][0] = v.x;
+              x[k][1] = v.y;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) x[k][e] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = i0 + k;
+          const float wk = __shfl_sync(0xffffffffu, i < 32 ? w0 : w1, i & 31);
+          if (i < p.n) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = fmaf(wk, x[k][e], acc[e]);
+          }
         }
       }
     }
