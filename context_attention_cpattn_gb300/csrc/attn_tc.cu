@@ -15,8 +15,10 @@
 // shared-memory slots.
 //
 // Warp roles (320 threads):
-//   warp 0      TMA producer: Q per item, then K_j and V_j through two-deep
-//               rings; K_j is refilled once S_j has read it, V_j once PV_j has.
+//   warp 0      TMA producer: Q per item, then K and V through two-deep
+//               rings in the order the MMAs read them (K_0, K_1, V_0, K_2,
+//               V_1, ...); K_j is refilled once S_j has read it, V_j once
+//               PV_j has.
 //   warp 1      TMEM allocator and MMA issuer (one thread).  TMEM holds two S
 //               buffers of 64 columns and O (128 columns).  Order per item:
 //                 S_0, S_1, PV_0, S_2, PV_1, S_3, ...
@@ -232,15 +234,28 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
         for (int kb = 0; kb < C::KB; ++kb)
           tma_load_3d(smem + kb * C::QBOX, &p.tm_q, q_full, kb * 64, it.h, tile.q_row0);
         issued[2] = ++qc;
+        // K_{j+1} goes before V_j, the order the MMAs consume them in (S_{j+1}
+        // is issued before PV_j); K_{j+1}'s buffer is free once S_{j-1} has
+        // run, which precedes PV_{j-2}, the MMA that frees V_j's buffer.
         PieceCursor c{tile.run_begin, 0, tile.run_end};
-        for (int j = 0; j < tile.n_kv_tiles; ++j, ++g) {
-          const int row = c.next(p.runs).row0;
-          const int b = g & 1;
-          if (g >= 2 && !wait_bounded(k_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 3)) { ok = false; break; }
+        auto load_k = [&](int gk, int row) -> bool {
+          const int b = gk & 1;
+          if (gk >= 2 && !wait_bounded(k_empty + b, ((gk >> 1) - 1) & 1, abort_flag, p.ws, 3)) return false;
           mbar_arrive_expect_tx(k_full + b, C::KV_BYTES);
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(smem + C::OFF_K + b * C::KV_BYTES + kb * C::KVBOX, &p.tm_k, k_full + b, kb * 64, it.g, row);
-          issued[0] = g + 1;
+          issued[0] = gk + 1;
+          return true;
+        };
+        int row_next = c.next(p.runs).row0;
+        if (!load_k(g, row_next)) break;
+        for (int j = 0; j < tile.n_kv_tiles; ++j, ++g) {
+          const int row = row_next;
+          const int b = g & 1;
+          if (j + 1 < tile.n_kv_tiles) {
+            row_next = c.next(p.runs).row0;
+            if (!load_k(g + 1, row_next)) { ok = false; break; }
+          }
           if (g >= 2 && !wait_bounded(v_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 4)) { ok = false; break; }
           mbar_arrive_expect_tx(v_full + b, C::KV_BYTES);
           for (int kb = 0; kb < C::KB; ++kb)
