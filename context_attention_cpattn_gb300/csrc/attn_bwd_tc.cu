@@ -18,18 +18,23 @@
 //
 // Persistent blocks, one per SM (all 512 TMEM columns):
 //   TMEM  S^T[2] (2 x 64) | dP^T (64) | dQ^T (64) | dV (128) | dK (128)
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warp 0      producer: K and V per item, Q_j and dO_j per piece through a
 //               two-deep ring (TMA), and the piece's -lse*log2(e) and -delta
 //               (plain loads by the 32 lanes) into shared memory.
-//   warp 1      TMEM allocator and MMA issuer (one thread), per piece j:
+//   warp 1      TMEM allocator and MMA issuer X (one thread), per piece j:
 //                 S^T_j  = K Q_j^T   (M=128 keys, N=64, K=D)        SS
 //                 dP^T_j = V dO_j^T  (M=128, N=64, K=D)             SS
+//   warp 10     MMA issuer Y (one thread), per piece j:
 //                 dV    += P^T_j dO_j (M=128, N=D, K=64)           TS, A = P^T from TMEM
-//                 S^T_{j+1} (into the other S buffer)
 //                 dK    += dS^T_j Q_j (M=128, N=D, K=64)           TS, A = dS^T from TMEM
 //                 dQ^T_j = K^T dS^T_j (M=D, N=64, K=128 keys)      SS, both MN-major
-//                 dP^T_{j+1}
+//               One thread cannot issue products with both operands in
+//               shared memory faster than about one per 96 cycles, well under
+//               the tensor pipe's rate; two issuing threads keep twice as many
+//               in flight.  X reuses S buffer j & 1 once Y's dV_{j-2} has read
+//               P^T_{j-2}, and the dP^T buffer once Y's dK_{j-1} has read
+//               dS^T_{j-1} (mbarriers committed by Y).
 //   warps 2-5   one key per thread: P^T from S^T (exp2 with the saved LSE,
 //               causal mask from token positions), written back to TMEM as
 //               bf16; dS^T from dP^T, written to TMEM (for dK) and to shared
@@ -96,7 +101,7 @@ struct BwdCfg {
   static constexpr uint32_t DQS_BYTES = 64 * D * 4;          // dQ staging tile (fp32)
   static constexpr uint32_t OFF_DQS = OFF_LD + 1024;          // dQ staging [2]
   static constexpr uint32_t OFF_BAR = OFF_DQS + 2 * DQS_BYTES;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;         // 31 mbarriers (248 bytes) below
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 512;         // 35 mbarriers (280 bytes) below
   static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;      // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 192, TM_DV = 256, TM_DK = 384;
@@ -134,7 +139,7 @@ struct Item {
 __device__ __forceinline__ Item item_of(int i, int n_tiles) { return Item{i % n_tiles, i / n_tiles}; }
 
 template <int D, bool kAccum>
-__global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   constexpr uint32_t IDESC_ST = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_KV = idesc_bf16_f32(128, D, false, true);
@@ -162,6 +167,9 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
   uint64_t* item_empty = bars + 23;  // [4]
   uint64_t* stage_full = bars + 27;  // [2] the dQ staging tile is written
   uint64_t* stage_free = bars + 29;  // [2] its previous reduce has read it
+  uint64_t* s_free = bars + 31;      // [2] dV_j has read P^T_j: S buffer j & 1 may be overwritten
+  uint64_t* dp_free = bars + 33;     // dK_j has read dS^T_j: the dP^T buffer may be overwritten
+  uint64_t* drain_y = bars + 34;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);     // loads issued: [0] K/V, [1] Q/dO
@@ -189,9 +197,13 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
     mbar_init(acc_done, 1);
     mbar_init(acc_free, 128);
     mbar_init(drain, 1);
+    mbar_init(drain_y, 1);
+    mbar_init(s_free, 1);
+    mbar_init(s_free + 1, 1);
+    mbar_init(dp_free, 1);
     for (int r = 0; r < 4; ++r) {
       mbar_init(item_full + r, 1);
-      mbar_init(item_empty + r, 257);  // MMA thread + 128 softmax + 128 dQ threads
+      mbar_init(item_empty + r, 258);  // two MMA threads + 128 softmax + 128 dQ threads
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(stage_full + b, 128);
@@ -289,11 +301,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer X
     if (lane == 0) {
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
-      const uint32_t sDS = smem_u32(smem + C::OFF_DS);
       // X^T_g = A B_g^T with A = K or V (K-major), B_g = Q or dO of piece g (K-major)
       auto issue_t = [&](uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
 #pragma unroll
@@ -304,7 +315,10 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
                        IDESC_ST, kk > 0 ? 1u : 0u);
         }
       };
-      int g = 0, kc = 0, ac = 0;
+      // S^T_j and dP^T_j, the products that read K and V from shared memory.
+      // S^T_j reuses the S buffer of piece j - 2 once dV_{j-2} has read its
+      // P^T; dP^T_j reuses the dP^T buffer once dK_{j-1} has read its dS^T.
+      int g = 0, kc = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int i = take_item(k, 5);
@@ -314,61 +328,20 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
         ok = wait_bounded(kv_full, kc & 1, abort_flag, p.ws, 6);
         if (!ok) break;
         ++kc;
-        {
+        for (int t = 0; ok && t < n; ++t, ++g) {
           const int b = g & 1;
           ok = wait_bounded(qd_full + b, (g >> 1) & 1, abort_flag, p.ws, 7);
+          if (ok && g >= 2) ok = wait_bounded(s_free + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 10);
           if (!ok) break;
           tc_fence_after();
           issue_t(tmem + C::TM_S + 64u * b, sK, sQ + b * C::QT_BYTES);
           umma_commit(s_full + b);
+          if (g >= 1) ok = wait_bounded(dp_free, (g - 1) & 1, abort_flag, p.ws, 23);
+          if (!ok) break;
+          tc_fence_after();
           issue_t(tmem + C::TM_DP, sV, sDO + b * C::QT_BYTES);
           umma_commit(dp_full);
         }
-        for (int t = 0; ok && t < n; ++t, ++g) {
-          const int b = g & 1;
-          ok = wait_bounded(p_full + b, (g >> 1) & 1, abort_flag, p.ws, 8);
-          // the item's first dV / dK overwrite the accumulators: the previous epilogue must have read them
-          if (ok && t == 0 && ac > 0) ok = wait_bounded(acc_free, (ac - 1) & 1, abort_flag, p.ws, 9);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t qb = sQ + b * C::QT_BYTES, dob = sDO + b * C::QT_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO: 16 queries per MMA
-            umma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + 64u * b + 8 * kk,
-                         smem_desc_sw128(dob + kk * 2048, C::QBOX, 1024), IDESC_KV, (t > 0 || kk > 0) ? 1u : 0u);
-          if (t + 1 < n) {
-            const int b1 = (g + 1) & 1;
-            ok = wait_bounded(qd_full + b1, ((g + 1) >> 1) & 1, abort_flag, p.ws, 10);
-            if (!ok) break;
-            tc_fence_after();
-            issue_t(tmem + C::TM_S + 64u * b1, sK, sQ + b1 * C::QT_BYTES);
-            umma_commit(s_full + b1);
-          }
-          ok = wait_bounded(ds_full, g & 1, abort_flag, p.ws, 11);
-          if (ok && g > 0) ok = wait_bounded(dq_free, (g - 1) & 1, abort_flag, p.ws, 12);
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q
-            umma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + 8 * kk, smem_desc_sw128(qb + kk * 2048, C::QBOX, 1024),
-                         IDESC_KV, (t > 0 || kk > 0) ? 1u : 0u);
-          const uint32_t dsb = sDS + b * C::DS_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T: 16 keys per MMA
-            umma_bf16_ss(tmem + C::TM_DQ, smem_desc_sw128(sK + kk * 2048, C::KBOX, 1024),
-                         smem_desc_sw128(dsb + kk * 2048, C::DS_BYTES, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
-          umma_commit(qd_empty + b);
-          umma_commit(dq_full);
-          if (t == n - 1) {
-            umma_commit(acc_done);
-            umma_commit(kv_empty);
-          } else {
-            const int b1 = (g + 1) & 1;
-            issue_t(tmem + C::TM_DP, sV, sDO + b1 * C::QT_BYTES);
-            umma_commit(dp_full);
-          }
-        }
-        ++ac;
       }
       umma_commit(drain);
       drain_wait(drain, 0);
@@ -522,7 +495,7 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
         ++ac;
       }
     }
-  } else {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ dQ (one head-dim column per thread)
     const int quad = warp & 3;
     const int d = quad * 32 + lane;
@@ -578,6 +551,63 @@ __global__ void __launch_bounds__(320, 1) attn_bwd_tc_kernel(const __grid_consta
     }
     // every reduce has finished before the block exits
     if (leader) bulk_wait_group_all();
+  } else {
+    // ------------------------------------------------------------ MMA issuer Y
+    // dV_j, dK_j and dQ^T_j: the products that read P^T_j and dS^T_j.  A second
+    // issuing thread, so that the shared-memory operand products of the two
+    // threads are in flight together.
+    if (lane == 0) {
+      const uint32_t sK = smem_u32(smem + C::OFF_K);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+      const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+      int g = 0, ac = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int i = take_item(k, 24);
+        if (i < 0) break;
+        const int n = p.tiles[item_of(i, p.n_tiles).tile_id].n_kv_tiles * G;
+        if (n == 0) continue;
+        for (int t = 0; ok && t < n; ++t, ++g) {
+          const int b = g & 1;
+          ok = wait_bounded(p_full + b, (g >> 1) & 1, abort_flag, p.ws, 8);
+          // the item's first dV / dK overwrite the accumulators: the previous epilogue must have read them
+          if (ok && t == 0 && ac > 0) ok = wait_bounded(acc_free, (ac - 1) & 1, abort_flag, p.ws, 9);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t qb = sQ + b * C::QT_BYTES, dob = sDO + b * C::QT_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // dV += P^T dO: 16 queries per MMA
+            umma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + 64u * b + 8 * kk,
+                         smem_desc_sw128(dob + kk * 2048, C::QBOX, 1024), IDESC_KV, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(s_free + b);
+          ok = wait_bounded(ds_full, g & 1, abort_flag, p.ws, 11);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q
+            umma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + 8 * kk, smem_desc_sw128(qb + kk * 2048, C::QBOX, 1024),
+                         IDESC_KV, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(dp_free);
+          if (g > 0) ok = wait_bounded(dq_free, (g - 1) & 1, abort_flag, p.ws, 12);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t dsb = sDS + b * C::DS_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T: 16 keys per MMA
+            umma_bf16_ss(tmem + C::TM_DQ, smem_desc_sw128(sK + kk * 2048, C::KBOX, 1024),
+                         smem_desc_sw128(dsb + kk * 2048, C::DS_BYTES, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
+          umma_commit(qd_empty + b);
+          umma_commit(dq_full);
+          if (t == n - 1) {
+            umma_commit(acc_done);
+            umma_commit(kv_empty);
+          }
+        }
+        ++ac;
+      }
+      umma_commit(drain_y);
+      drain_wait(drain_y, 0);
+    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -670,7 +700,7 @@ cudaError_t launch_bwd_tc(const BwdParams& p, int n_blocks, cudaStream_t stream)
   const uint32_t smem = BwdCfg<D>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<n_blocks, 320, smem, stream>>>(p);
+  kern<<<n_blocks, 352, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
