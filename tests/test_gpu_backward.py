@@ -246,3 +246,7 @@ def test_long_video_200k_backward_full_size(cp):
 
 def test_video_latent_grid2d_backward_full_size(cp):
     _full_size_single_sequence(cp, "video_latent_grid2d", 256)
+
+
+def test_single_seq_1m_backward_full_size(cp):
+    _full_size_single_sequence(cp, "single_seq_1m_gqa", 24)
