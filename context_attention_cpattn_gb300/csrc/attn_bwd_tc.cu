@@ -101,7 +101,7 @@ struct BwdCfg {
   static constexpr uint32_t DQS_BYTES = 64 * D * 4;          // dQ staging tile (fp32)
   static constexpr uint32_t OFF_DQS = OFF_LD + 1024;          // dQ staging [2]
   static constexpr uint32_t OFF_BAR = OFF_DQS + 2 * DQS_BYTES;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 512;         // 35 mbarriers (280 bytes) below
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 512;         // 36 mbarriers (288 bytes) below
   static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;      // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 192, TM_DV = 256, TM_DK = 384;
@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
   uint64_t* s_free = bars + 31;      // [2] dV_j has read P^T_j: S buffer j & 1 may be overwritten
   uint64_t* dp_free = bars + 33;     // dK_j has read dS^T_j: the dP^T buffer may be overwritten
   uint64_t* drain_y = bars + 34;
+  uint64_t* ds_smem_full = bars + 35;  // dS^T_j's shared-memory copy (B of dQ^T) is written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);     // loads issued: [0] K/V, [1] Q/dO
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
     mbar_init(s_free, 1);
     mbar_init(s_free + 1, 1);
     mbar_init(dp_free, 1);
+    mbar_init(ds_smem_full, 128);
     for (int r = 0; r < 4; ++r) {
       mbar_init(item_full + r, 1);
       mbar_init(item_empty + r, 258);  // two MMA threads + 128 softmax + 128 dQ threads
@@ -425,6 +427,9 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
           }
         }
         tmem_st32(tl + C::TM_DP, ds);  // dS^T (A of dK) over the first 32 columns of dP^T
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(ds_full);  // dK_j may start; dQ^T_j waits for the copy below
         // dS^T for dQ^T: this buffer was last read by the dQ^T MMA of piece g - 2
         if (g >= 2 &&
             !__all_sync(0xffffffffu, wait_bounded(qd_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 17))) {
@@ -438,9 +443,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
             st_shared_v4(rbase + ((c ^ (row & 7)) << 4), ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
         }
         fence_proxy_async_smem();
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(ds_full);
+        mbar_arrive(ds_smem_full);
       }
       if (!ok) break;
 
@@ -589,6 +592,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
                          IDESC_KV, (t > 0 || kk > 0) ? 1u : 0u);
           umma_commit(dp_free);
           if (g > 0) ok = wait_bounded(dq_free, (g - 1) & 1, abort_flag, p.ws, 12);
+          if (ok) ok = wait_bounded(ds_smem_full, g & 1, abort_flag, p.ws, 25);
           if (!ok) break;
           tc_fence_after();
           const uint32_t dsb = sDS + b * C::DS_BYTES;
