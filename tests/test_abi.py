@@ -93,3 +93,73 @@ def test_workspace_size_grows_with_grid_shards(cpattn):
     assert 256 < wz < (1 << 22)
     T = 16 * 45 * 80
     assert wg >= T * 8 + 3 * T * 24 * 128 * 2
+
+
+def test_backward_and_mesh_argument_errors(cpattn):
+    """Every rejection below happens in the host-side checks, before any
+    device call (the pointers are never dereferenced)."""
+    L = cpattn.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    ws = ctypes.c_void_p(1 << 20)
+    plan = cpattn.cpattn_plan([0, 256], 2, "zigzag")
+    bf, f32 = cpattn.DTYPE_BF16, cpattn.DTYPE_FP32
+
+    def bwd(p=plan, dtype=bf, H=4, Hkv=4, D=128, scale=0.1, causal=1, o=fake, dq=fake, ws_ptr=ws, ws_bytes=1 << 30):
+        return L.cpattn_bwd(p.handle, fake, fake, fake, o, fake, fake, dtype, H, Hkv, D, scale, causal, dq, fake,
+                            fake, ws_ptr, ws_bytes, None)
+
+    assert bwd(D=64) == cpattn.UNSUPPORTED                      # bf16 backward needs D = 128
+    assert bwd(dtype=f32, D=96) == cpattn.UNSUPPORTED           # head dim
+    assert bwd(H=6) == cpattn.INVALID_ARG                       # H not a multiple of Hkv
+    assert bwd(o=None) == cpattn.INVALID_ARG                    # NULL O
+    assert bwd(dq=ctypes.c_void_p((1 << 20) + 8)) == cpattn.INVALID_ARG  # misaligned dQ
+    assert bwd(scale=0.0) == cpattn.INVALID_ARG
+    assert bwd(scale=float("inf")) == cpattn.INVALID_ARG
+    assert bwd(ws_ptr=ctypes.c_void_p((1 << 20) + 64)) == cpattn.WORKSPACE
+    assert bwd(ws_bytes=64) == cpattn.WORKSPACE
+    assert b"workspace too small" in L.cpattn_last_error_string()
+    # per-step backward: rank and step ranges
+    s = L.cpattn_block_bwd(plan.handle, fake, fake, fake, fake, fake, fake, bf, 4, 4, 128, 0.1, 1, 2, 0, fake, fake,
+                           fake, ws, 1 << 30, None)
+    assert s == cpattn.INVALID_ARG
+    s = L.cpattn_block_bwd(plan.handle, fake, fake, fake, fake, fake, fake, bf, 4, 4, 128, 0.1, 1, 0, -1, fake, fake,
+                           fake, ws, 1 << 30, None)
+    assert s == cpattn.INVALID_ARG
+    out = ctypes.c_size_t()
+    # causal grid2d has no backward either
+    gplan = cpattn.cpattn_plan([0, 2 * 9 * 20], 4, "grid2d", (2, 9, 20))
+    assert L.cpattn_bwd_workspace_size(gplan.handle, 2, 2, 128, bf, 1, ctypes.byref(out)) == cpattn.UNSUPPORTED
+    assert L.cpattn_bwd_workspace_size(gplan.handle, 2, 2, 128, bf, 0, ctypes.byref(out)) == cpattn.OK
+    # mesh and paired plans: whole forward only; heads must split over the Ulysses degree
+    mesh = cpattn.cpattn_plan_2d([0, 300, 557, 1200], 2, 2)
+    assert L.cpattn_bwd_workspace_size(mesh.handle, 8, 4, 128, bf, 1, ctypes.byref(out)) == cpattn.UNSUPPORTED
+    assert bwd(p=mesh, H=8, Hkv=4) == cpattn.UNSUPPORTED
+    s = L.cpattn_fwd(mesh.handle, fake, fake, fake, bf, 6, 3, 128, 0.1, 1, fake, fake, ws, 1 << 30, None)
+    assert s == cpattn.UNSUPPORTED                              # 3 KV heads over u = 2
+    s = L.cpattn_block_fwd(mesh.handle, fake, fake, fake, bf, 8, 4, 128, 0.1, 1, 0, 0, fake, fake, ws, 1 << 30, None)
+    assert s == cpattn.UNSUPPORTED
+    paired = cpattn.cpattn_plan_paired([0, 64], 2, 4)
+    s = L.cpattn_fwd(paired.handle, fake, fake, fake, bf, 4, 4, 128, 0.1, 0, fake, fake, ws, 1 << 30, None)
+    assert s == cpattn.UNSUPPORTED                              # the teacher-forcing mask needs causal = 1
+
+
+@pytest.mark.parametrize("args", [
+    ([0, 100], 0, 2),        # ulysses < 1
+    ([0, 100], 2, 0),        # ring < 1
+    ([0, 3], 1, 2),          # a sequence shorter than 2 * ring
+])
+def test_mesh_plan_rejects_bad_inputs(cpattn, args):
+    with pytest.raises(cpattn.CpattnError) as e:
+        cpattn.cpattn_plan_2d(*args)
+    assert e.value.status == cpattn.INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [
+    ([0, 41], 2, 4),         # odd sample length: no clean/noisy halves
+    ([0, 40], 3, 4),         # chunks not a multiple of cp
+    ([0, 6], 2, 4),          # fewer tokens per stream than chunks
+])
+def test_paired_plan_rejects_bad_inputs(cpattn, args):
+    with pytest.raises(cpattn.CpattnError) as e:
+        cpattn.cpattn_plan_paired(*args)
+    assert e.value.status == cpattn.INVALID_ARG
