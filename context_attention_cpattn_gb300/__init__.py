@@ -59,6 +59,7 @@ _SIGNATURES = {
     "cpattn_plan_allowed_pairs": [_P, _I32, _P],
     "cpattn_plan_destroy": [_P],
     "cpattn_plan_get_a2a_map": [_P, _P, _I64],
+    "cpattn_plan_get_worklist": [_P, _I32, _I32, _I32, _I32, _I32, _P, _I64, _P, _I64, _P, _P],
     "cpattn_plan_get_info": [_P, _P],
     "cpattn_plan_get_chunk_offsets": [_P, _P, _I64],
     "cpattn_plan_get_chunk_ranks": [_P, _P, _I64],
@@ -181,6 +182,19 @@ class Plan:
     def a2a_map(self):
         """ULYSSES2D and PAIRED plans: the all-to-all row gather map [u*T]."""
         return self._get("cpattn_plan_get_a2a_map", self.info()["split_h"] * int(self.cu_seqlens[-1]), np.int64)
+
+    def worklist(self, backward: bool, dtype, causal: bool = True, q_rank: int = -1, ring_step: int = 0):
+        """The work list a call hands its kernel: (tiles int32 [n, 8] with
+        columns row0, pos0, out_row0, rows, run_begin, run_end, pieces, rank;
+        runs int32 [m, 4] with columns row0, pos0, len, masked)."""
+        args = (self._h, int(bool(backward)), _dtype_code_of(dtype), int(bool(causal)), int(q_rank), int(ring_step))
+        nt, nr = ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().cpattn_plan_get_worklist(*args, None, 0, None, 0, ctypes.byref(nt), ctypes.byref(nr)))
+        tiles = np.zeros((nt.value, 8), dtype=np.int32)
+        runs = np.zeros((nr.value, 4), dtype=np.int32)
+        _check(lib().cpattn_plan_get_worklist(*args, tiles.ctypes.data, nt.value, runs.ctypes.data, nr.value,
+                                              ctypes.byref(nt), ctypes.byref(nr)))
+        return tiles, runs
 
     def ring_schedule(self, causal: bool):
         n = self.cp * self.cp

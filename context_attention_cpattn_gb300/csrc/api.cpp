@@ -454,6 +454,51 @@ cpattn_status_t cpattn_workspace_size(const cpattn_plan_t* plan, int32_t H, int3
   return CPATTN_OK;
 }
 
+cpattn_status_t cpattn_plan_get_worklist(const cpattn_plan_t* cplan, int32_t backward, cpattn_dtype_t dtype,
+                                         int32_t causal, int32_t q_rank, int32_t ring_step,
+                                         cpattn_work_tile_t* tiles, int64_t max_tiles, cpattn_work_run_t* runs,
+                                         int64_t max_runs, int64_t* n_tiles, int64_t* n_runs) {
+  if (!cplan || !n_tiles || !n_runs) return fail(CPATTN_INVALID_ARG, "NULL argument");
+  if (dtype != CPATTN_DTYPE_FP32 && dtype != CPATTN_DTYPE_BF16) return fail(CPATTN_UNSUPPORTED, "dtype must be fp32 or bf16");
+  if (causal && cplan->mode == CPATTN_MODE_GRID2D)
+    return fail(CPATTN_UNSUPPORTED, "causal masks are not defined for grid2d plans");
+  if (cplan->mode == CPATTN_MODE_PAIRED && !causal)
+    return fail(CPATTN_UNSUPPORTED, "paired plans apply the teacher-forcing mask (causal must be 1)");
+  if (head_sharded(cplan->mode) && (backward || q_rank >= 0))
+    return fail(CPATTN_UNSUPPORTED, "ulysses2d and paired plans run the whole forward only (cpattn_fwd)");
+  if (q_rank >= cplan->cp || q_rank < -1) return fail(CPATTN_INVALID_ARG, "q_rank out of range");
+  if (q_rank >= 0 && (ring_step < 0 || ring_step >= cplan->cp)) return fail(CPATTN_INVALID_ARG, "ring_step out of range");
+  cpattn_plan_t* plan = const_cast<cpattn_plan_t*>(cplan);
+  const int step = q_rank >= 0 ? ring_step : 0;
+  std::shared_ptr<const WorkList> wl;
+  if (backward) {
+    int tk, tq;
+    bwd_tile_sizes(dtype, &tk, &tq);
+    wl = cpattn::get_worklist_bwd(*plan, causal != 0, tk, tq, q_rank, step);
+  } else {
+    int tm, tn;
+    bool pair;
+    tile_sizes(dtype, &tm, &tn, &pair);
+    wl = cpattn::get_worklist(*plan, causal != 0, tm, tn, pair, q_rank, step);
+  }
+  *n_tiles = (int64_t)wl->tiles.size();
+  *n_runs = (int64_t)wl->runs.size();
+  if ((tiles && max_tiles < *n_tiles) || (runs && max_runs < *n_runs))
+    return fail(CPATTN_INVALID_ARG, "output too small");
+  if (tiles)
+    for (size_t i = 0; i < wl->tiles.size(); ++i) {
+      const QTile& t = wl->tiles[i];
+      tiles[i] = cpattn_work_tile_t{t.q_row0, t.q_pos0, t.out_row0, t.q_rows, t.run_begin, t.run_end, t.n_kv_tiles,
+                                    t.rank};
+    }
+  if (runs)
+    for (size_t i = 0; i < wl->runs.size(); ++i) {
+      const KvRun& r = wl->runs[i];
+      runs[i] = cpattn_work_run_t{r.kv_row0, r.kv_pos0, r.kv_len, r.causal};
+    }
+  return CPATTN_OK;
+}
+
 static cpattn_status_t run_attention(const cpattn_plan_t* cplan, const void* q, const void* k, const void* v,
                                      cpattn_dtype_t dtype, int32_t H, int32_t Hkv, int32_t D, float scale,
                                      int32_t causal, int q_rank, int step, void* o, float* lse, void* workspace,

@@ -212,6 +212,42 @@ cpattn_status_t cpattn_plan_get_ring_schedule(const cpattn_plan_t* plan, int32_t
  * Other plans: CPATTN_INVALID_ARG. */
 cpattn_status_t cpattn_plan_get_a2a_map(const cpattn_plan_t* plan, int64_t* out, int64_t n);
 
+/* The work list a call hands its kernel, as a host copy (so the planner can
+ * be checked against the mask's definition without a GPU).
+ *   backward = 0: the query tiles of cpattn_fwd (q_rank = -1) or of
+ *     cpattn_block_fwd(q_rank, ring_step), each with the key runs it reads,
+ *     in ring order (at step t the queries of rank r read the KV shard of
+ *     rank (r - t) mod cp).
+ *   backward = 1: the key tiles of cpattn_bwd / cpattn_block_bwd, each with
+ *     the query runs that see it, in ring order (the KV shard of rank k
+ *     meets the queries of rank (k + t) mod cp at step t).
+ * Tile and piece sizes are those of the kernel for `dtype`.
+ *   tile: row0, pos0, rows = its rows (buffer row, position inside the
+ *     sequence (GRID2D, bidirectional only: the gathered row), count);
+ *     out_row0 = output row of the first; runs
+ *     [run_begin, run_end); pieces = kernel loop trips over its runs; rank =
+ *     the virtual rank that owns the tile.
+ *   run: row0, pos0, len = rows of the other side; masked = 1 when the
+ *     position mask (key position <= query position) applies inside the run,
+ *     0 when every pair of the tile and the run is allowed.
+ * Rows are rows of the buffers the kernel reads: global rows, for GRID2D the
+ * gathered rank-major rows of the index map, for ULYSSES2D and PAIRED the
+ * rows of the head-sharded buffers (head group i at i*T).  *n_tiles and
+ * *n_runs receive the counts; tiles and runs (capacities max_tiles,
+ * max_runs) may be NULL to ask for the counts only.  Errors: those of the
+ * call described (unsupported plan, mode or causal flag, rank or step out of
+ * range); CPATTN_INVALID_ARG when a buffer is smaller than its count. */
+typedef struct cpattn_work_tile_t {
+  int32_t row0, pos0, out_row0, rows, run_begin, run_end, pieces, rank;
+} cpattn_work_tile_t;
+typedef struct cpattn_work_run_t {
+  int32_t row0, pos0, len, masked;
+} cpattn_work_run_t;
+cpattn_status_t cpattn_plan_get_worklist(const cpattn_plan_t* plan, int32_t backward, cpattn_dtype_t dtype,
+                                         int32_t causal, int32_t q_rank, int32_t ring_step,
+                                         cpattn_work_tile_t* tiles, int64_t max_tiles, cpattn_work_run_t* runs,
+                                         int64_t max_runs, int64_t* n_tiles, int64_t* n_runs);
+
 /* ---------------------------------------------------------------- attention */
 
 /* Bytes of device workspace that cpattn_fwd / cpattn_block_fwd need for this
