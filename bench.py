@@ -470,11 +470,31 @@ def run_ours(args, rep: Replicas):
         "fwd_ms_mean": 1e3 * fwd_mean_s,
         "fwd_ms_min": min(fwd_ms),
         "tc_source_sha256": tc_source_hash(),
+        "mma_area_useful": useful_mma_fraction(plan, w.causal, w.dtype),
     }
     if not args.no_cpu_baseline and rep.world == 1 and w.mode != "paired":
         # (the CPU legs evaluate the causal / bidirectional oracle; paired plans use another mask)
         line["cpu_baseline"] = run_cpu_baseline(args)
     print(json.dumps(line), flush=True)
+
+
+# Kernel tile shapes (rows per tile, keys or queries per piece) of the bf16 and
+# fp32 forward and backward kernels.
+TILE_SHAPES = {(False, "bf16"): (128, 64), (False, "fp32"): (64, 32),
+               (True, "bf16"): (128, 64), (True, "fp32"): (32, 64)}
+
+
+def useful_mma_fraction(plan, causal: bool, dtype: str = "bf16", backward: bool = False):
+    """Share of a kernel's executed tile area (per query head) that falls on
+    pairs the mask allows: allowed pairs over the tile area summed over the
+    work list the call uploads (one head group's copy for head-sharded plans).
+    The rest is the padding of partial tiles and pieces and the masked-out
+    triangles of diagonal tiles."""
+    tiles, _ = plan.worklist(backward, dtype, causal)
+    tm, tn = TILE_SHAPES[(backward, dtype)]
+    executed = int(tiles[:, 6].astype(np.int64).sum()) * tm * tn
+    groups = plan.info()["split_h"] if plan.mode in (3, 4) else 1   # ulysses2d, paired
+    return groups * plan.allowed_pairs(causal) / executed if executed else None
 
 
 def run_bwd(args):
@@ -536,7 +556,8 @@ def run_bwd(args):
                      "peak_source": peak_src,
                      "traffic": recorded_traffic(w.name, BWD_TRAFFIC_FILE, BWD_SOURCES),
                      "kernel": "cpattn_bwd call (pre + attn_bwd_tc_kernel + post), CUDA events per call"},
-        "gpu_launches": launches * args.steps, "clocks": clocks}), flush=True)
+        "gpu_launches": launches * args.steps, "clocks": clocks,
+        "mma_area_useful": useful_mma_fraction(plan, w.causal, w.dtype, backward=True)}), flush=True)
 
 
 def measured_hbm() -> tuple[float, str]:

@@ -72,3 +72,20 @@ def test_row_flops_counts_real_lengths():
     rows = np.array([0, 9, 10, 29])
     assert bench.row_flops(cu, rows, 2, 4, True) == 4 * 4 * 2 * (1 + 10 + 1 + 20)
     assert bench.row_flops(cu, rows, 2, 4, False) == 4 * 4 * 2 * (10 + 10 + 20 + 20)
+
+
+def test_useful_mma_area_of_the_workloads(cpattn):
+    """The bench line's useful share of the forward kernel's tile area: about
+    0.69 on the micro-batch (short zigzag chunks), near 1 on one long sequence."""
+    import inputs
+    w = inputs.workload("dynamic_cp_microbatch")
+    plan = cpattn.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
+    f = bench.useful_mma_fraction(plan, True)
+    assert 0.69 < f < 0.70
+    assert 0.69 < bench.useful_mma_fraction(plan, True, backward=True) < 0.71
+    one = cpattn.cpattn_plan([0, 4096], 2, "zigzag")
+    # 4096 tokens, 4 chunks of 1024: only each tile's diagonal 128 x 128 block is
+    # partly masked, about half of it over a mean of ~2,100 keys per tile row
+    assert 0.96 < bench.useful_mma_fraction(one, True) < 0.98
+    full = cpattn.cpattn_plan([0, 4096], 2, "zigzag")
+    assert bench.useful_mma_fraction(full, False) == 1.0
