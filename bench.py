@@ -123,6 +123,11 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+def clock_csv_path(tag: str) -> str:
+    """Where the raw clock samples go: the directory in CPATTN_CLOCKS_DIR, else /tmp."""
+    return os.path.join(os.environ.get("CPATTN_CLOCKS_DIR", "/tmp"), f"cpattn_clocks_{tag}.csv")
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -350,8 +355,7 @@ def run_ours(args, rep: Replicas):
         step()
     cp.cpattn_sync_status(ws, stream)
 
-    sampler = ClockSampler(rep.local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rep.rank}.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/cpattn_clocks_{rep.rank}.csv")
+    sampler = ClockSampler(rep.local, clock_csv_path(f"rank{rep.rank}"))
     fwd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     rep.barrier()
@@ -531,8 +535,7 @@ def run_bwd(args):
     for _ in range(args.warmup):
         step()
     cp.cpattn_sync_status(ws, stream)
-    sampler = ClockSampler(0, os.path.join(ROOT, "gpurun_out", "clocks_bwd.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp/cpattn_clocks_bwd.csv")
+    sampler = ClockSampler(0, clock_csv_path("bwd"))
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     torch.cuda.synchronize(dev)
     for a, b in ev:
