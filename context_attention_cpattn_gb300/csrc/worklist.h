@@ -46,5 +46,3 @@ typedef struct WsHeader {
 #endif
 
 #define CPATTN_FAULT_WAIT_TIMEOUT 1u
-#define CPATTN_FAULT_BAD_INDEX 2u
-#define CPATTN_FAULT_TMEM 3u

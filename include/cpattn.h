@@ -41,10 +41,10 @@
  *     Plans are host objects owned by the library, freed with
  *     cpattn_plan_destroy().
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device work
- *     is asynchronous; argument errors are reported synchronously.  A kernel
- *     that detects a fault (a bounded wait that ran out, a bad index) records
- *     it in the workspace and returns early; cpattn_sync_status() reports it
- *     as CPATTN_DEVICE_FAULT.
+ *     is asynchronous; argument errors are reported synchronously.  Every
+ *     wait inside a kernel is bounded: one that runs out records a fault in
+ *     the workspace and the kernel returns early; cpattn_sync_status()
+ *     reports it as CPATTN_DEVICE_FAULT.
  */
 #ifndef CPATTN_H
 #define CPATTN_H
