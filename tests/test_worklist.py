@@ -200,3 +200,51 @@ def test_worklist_rejects_what_the_calls_reject(cpattn):
     p = cpattn.cpattn_plan_paired([0, 96, 256], 4, 8)
     with pytest.raises(cpattn.CpattnError):
         p.worklist(False, "bf16", False)           # the teacher-forcing mask needs causal
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_layouts(cpattn, seed):
+    """Seeded random lengths, CP sizes, grids and meshes: every list visits
+    every allowed pair once."""
+    rng = np.random.default_rng(1000 + seed)
+    for cp in (1, 2, 3, 4, 8):
+        lens = rng.integers(2 * cp, 260, size=rng.integers(1, 6))
+        cu = tuple(int(x) for x in np.concatenate([[0], np.cumsum(lens)]))
+        seq, pos = seq_pos(cu)
+        for mode in ("zigzag", "contiguous"):
+            plan = cpattn.cpattn_plan(cu, cp, mode)
+            tok_of_row, rank_of_tok, _ = rank_maps(plan, False)
+            for causal in (True, False):
+                for backward in (False, True):
+                    dtype = ("bf16", "fp32")[int(rng.integers(0, 2))]
+                    rows, piece = (BWD_TILES if backward else FWD_TILES)[dtype]
+                    tiles, runs = plan.worklist(backward, dtype, causal)
+                    count, seen = replay(tiles, runs, tok_of_row, seq, pos, causal, rows, piece, backward,
+                                         rank_of_tok, cp)
+                    assert (seen == 1).all()
+                    assert np.array_equal(count, definition(cu, causal).astype(np.int32)), (cu, cp, mode, causal)
+    for cp in (2, 4, 6, 8):
+        F, h, w = (int(x) for x in (rng.integers(1, 3), rng.integers(4, 16), rng.integers(4, 16)))
+        try:
+            plan = cpattn.cpattn_plan([0, F * h * w], cp, "grid2d", (F, h, w))
+        except cpattn.CpattnError:
+            continue                                  # a side too short for its pieces
+        cu = (0, F * h * w)
+        seq, pos = seq_pos(cu)
+        tok_of_row, rank_of_tok, _ = rank_maps(plan, True)
+        for backward in (False, True):
+            rows, piece = (BWD_TILES if backward else FWD_TILES)["bf16"]
+            tiles, runs = plan.worklist(backward, "bf16", False)
+            count, seen = replay(tiles, runs, tok_of_row, seq, pos, False, rows, piece, backward, rank_of_tok, cp,
+                                 gathered=True)
+            assert (seen == 1).all() and np.array_equal(count, definition(cu, False).astype(np.int32))
+    for u, r in ((2, 2), (4, 1), (1, 4), (2, 3)):
+        lens = rng.integers(2 * r, 240, size=rng.integers(1, 5))
+        cu = tuple(int(x) for x in np.concatenate([[0], np.cumsum(lens)]))
+        plan = cpattn.cpattn_plan_2d(cu, u, r)
+        T = cu[-1]
+        seq, pos = seq_pos(cu)
+        tok_of_row = plan.index_map()[np.arange(u * T) % T]
+        tiles, runs = plan.worklist(False, "bf16", True)
+        count, seen = replay(tiles, runs, tok_of_row, seq, pos, True, 128, 64, False)
+        assert (seen == u).all() and np.array_equal(count, u * definition(cu, True).astype(np.int32)), (cu, u, r)
