@@ -18,6 +18,8 @@ from typing import Optional, Sequence
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
+# CPATTN_LIB loads another prebuilt copy of the library instead of the in-tree
+# one (build() always writes the in-tree library).
 LIB_PATH = os.environ.get("CPATTN_LIB") or os.path.join(_PKG, "lib", "libcpattn.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "cpattn.h")
 

@@ -16,7 +16,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
-LIB = os.environ.get("CPATTN_LIB") or os.path.join(PKG, "lib", "libcpattn.so")
+LIB = os.path.join(PKG, "lib", "libcpattn.so")   # always the in-tree library (CPATTN_LIB only picks what loads)
 
 SOURCES = ["api.cpp", "plan.cpp", "attn_tc.cu", "attn_simt.cu", "merge.cu", "loss.cu", "permute.cu", "static_scratch.cu", "dcp.cpp", "attn_bwd_tc.cu", "attn_bwd_simt.cu", "tensor_map.cpp"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
