@@ -163,3 +163,18 @@ def test_paired_plan_rejects_bad_inputs(cpattn, args):
     with pytest.raises(cpattn.CpattnError) as e:
         cpattn.cpattn_plan_paired(*args)
     assert e.value.status == cpattn.INVALID_ARG
+
+
+def test_every_plan_entry_point_rejects_a_null_plan(cpattn):
+    """NULL plan, NULL pointers and zero sizes: each call returns
+    CPATTN_INVALID_ARG without touching memory (destroy of NULL is a no-op)."""
+    L = cpattn.lib()
+    names = [n for n in cpattn._SIGNATURES if n.startswith("cpattn_plan_get") or n in (
+        "cpattn_workspace_size", "cpattn_fwd", "cpattn_block_fwd", "cpattn_bwd_workspace_size", "cpattn_bwd",
+        "cpattn_block_bwd", "cpattn_fwd_static", "cpattn_plan_allowed_pairs")]
+    assert len(names) >= 17
+    for n in names:
+        sig = cpattn._SIGNATURES[n]
+        args = [None] + [None if t is ctypes.c_void_p else 0 for t in sig[1:]]
+        assert getattr(L, n)(*args) == cpattn.INVALID_ARG, n
+    assert L.cpattn_plan_destroy(None) == cpattn.OK
