@@ -178,3 +178,22 @@ def test_every_plan_entry_point_rejects_a_null_plan(cpattn):
         args = [None] + [None if t is ctypes.c_void_p else 0 for t in sig[1:]]
         assert getattr(L, n)(*args) == cpattn.INVALID_ARG, n
     assert L.cpattn_plan_destroy(None) == cpattn.OK
+
+
+def test_merge_permute_and_loss_argument_errors(cpattn):
+    L = cpattn.lib()
+    fake = ctypes.c_void_p(1 << 20)
+    arr = (ctypes.c_void_p * 2)(1 << 20, 1 << 21)
+    bf = cpattn.DTYPE_BF16
+    assert L.cpattn_merge(0, arr, arr, 10, 4, 128, None, 10, fake, bf, fake, None) == cpattn.INVALID_ARG
+    assert L.cpattn_merge(2, None, None, 10, 4, 128, None, 10, fake, bf, fake, None) == cpattn.INVALID_ARG
+    assert L.cpattn_merge(2, arr, arr, 10, 4, 96, None, 10, fake, bf, fake, None) == cpattn.UNSUPPORTED
+    assert L.cpattn_merge(2, arr, arr, -1, 4, 128, None, 10, fake, bf, fake, None) == cpattn.INVALID_ARG
+    assert L.cpattn_merge(2, arr, arr, 10, 4, 128, None, 5, fake, bf, fake, None) == cpattn.INVALID_ARG
+    assert L.cpattn_merge(2, arr, arr, 10, 4, 128, None, 10, None, bf, fake, None) == cpattn.INVALID_ARG
+    assert L.cpattn_gather_rows(fake, 10, fake, fake, 10, 24, None) == cpattn.INVALID_ARG      # row bytes % 16
+    assert L.cpattn_gather_rows(ctypes.c_void_p((1 << 20) + 4), 10, fake, fake, 10, 32, None) == cpattn.INVALID_ARG
+    assert L.cpattn_gather_rows(fake, 10, fake, None, 10, 32, None) == cpattn.INVALID_ARG
+    assert L.cpattn_scatter_rows(fake, fake, 10, fake, -3, 32, None) == cpattn.INVALID_ARG
+    assert L.cpattn_token_loss_norm(None, fake, 10, fake, fake, None, None) == cpattn.INVALID_ARG
+    assert L.cpattn_token_loss_norm(fake, fake, -1, fake, fake, None, None) == cpattn.INVALID_ARG
