@@ -52,11 +52,16 @@ def to_f64(x) -> np.ndarray:
 
 
 def _softmax_rows(S: np.ndarray, V: np.ndarray):
-    """Softmax-weighted sum for each row of S (masked entries are -inf)."""
+    """Softmax-weighted sum for each row of S (masked entries are -inf).
+
+    S is a temporary of the caller and is overwritten: S - m and its
+    exponential are formed in place (the same operations as out of place, with
+    fewer full-size temporaries)."""
     m = S.max(axis=1)
     ok = np.isfinite(m)
     m_safe = np.where(ok, m, 0.0)
-    P = np.exp(S - m_safe[:, None])
+    S -= m_safe[:, None]
+    P = np.exp(S, out=S)
     l = P.sum(axis=1)
     with np.errstate(divide="ignore", invalid="ignore"):
         O = (P @ V) / l[:, None]
@@ -132,7 +137,7 @@ def block_attention(q, k, v, cu_seqlens, q_rows, kv_rows, causal: bool, scale: f
 
 
 def attention_at_rows(q, k, v, cu_seqlens, rows, causal: bool, scale: float,
-                      threads: int | None = None, batch: int = 16):
+                      threads: int | None = None, batch: int | None = None):
     """Attention of the sampled query rows ``rows`` (all heads) over their full
     sequences; returns (O [R,H,D] fp64, LSE [H,R] fp64).
 
@@ -141,8 +146,9 @@ def attention_at_rows(q, k, v, cu_seqlens, rows, causal: bool, scale: float,
     full [T,H,D] tensor; ``k``/``v`` are full [T,Hkv,D] tensors (torch or
     numpy, any float dtype).  For each KV head and each sequence holding a
     sampled row, the keys up to the last sampled row are converted to fp64
-    once; independent row batches run on a thread pool (numpy releases the
-    GIL).
+    once; independent row batches run on one thread pool (numpy releases the
+    GIL).  The causal rule is applied by setting the scores of the keys after
+    each query's position to -inf.
     """
     rows = np.asarray(rows, dtype=np.int64)
     cu = np.asarray(cu_seqlens, dtype=np.int64)
@@ -156,30 +162,32 @@ def attention_at_rows(q, k, v, cu_seqlens, rows, causal: bool, scale: float,
     O = np.zeros((R, H, D))
     LSE = np.full((H, R), -np.inf)
     threads = threads or max(1, len(os.sched_getaffinity(0)))
-    for g in range(Hkv):
-        heads = [h for h in range(H) if kv_head(h, H, Hkv) == g]
-        assert len(heads) == G
-        for s in np.unique(seq):
-            idx_s = np.nonzero(seq == s)[0]
-            a, b = int(cu[s]), int(cu[s + 1])
-            kend_s = int(rows[idx_s].max()) + 1 if causal else b
-            k_s = to_f64(k[a:kend_s, g, :])   # keys of this sequence up to the last sampled row
-            v_s = to_f64(v[a:kend_s, g, :])
+    batch = batch or max(16, 128 // G)    # about 128 (row, head) pairs per matrix product
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for g in range(Hkv):
+            heads = [h for h in range(H) if kv_head(h, H, Hkv) == g]
+            assert len(heads) == G
+            for s in np.unique(seq):
+                idx_s = np.nonzero(seq == s)[0]
+                a, b = int(cu[s]), int(cu[s + 1])
+                kend_s = int(rows[idx_s].max()) + 1 if causal else b
+                k_s = to_f64(k[a:kend_s, g, :])   # keys of this sequence up to the last sampled row
+                v_s = to_f64(v[a:kend_s, g, :])
 
-            def work(idx, a=a, b=b, k_s=k_s, v_s=v_s):
-                rr = rows[idx]
-                kend = int(rr.max()) + 1 if causal else b
-                Qb = qr[idx][:, heads, :].reshape(len(idx) * G, D)
-                S = scale * (Qb @ k_s[: kend - a].T)
-                if causal:
-                    qpos = np.repeat(rr - a, G)[:, None]
-                    kpos = np.arange(kend - a)[None, :]
-                    S = np.where(causal_visible(kpos, qpos), S, -np.inf)
-                Ob, Lb = _softmax_rows(S, v_s[: kend - a])
-                return idx, Ob.reshape(len(idx), G, D), Lb.reshape(len(idx), G)
+                def work(idx, a=a, b=b, k_s=k_s, v_s=v_s):
+                    rr = rows[idx]
+                    kend = int(rr.max()) + 1 if causal else b
+                    Qb = qr[idx][:, heads, :].reshape(len(idx) * G, D)
+                    S = Qb @ k_s[: kend - a].T
+                    S *= scale
+                    if causal:
+                        for r, qpos in enumerate(np.repeat(rr - a, G)):
+                            S[r, qpos + 1:] = -np.inf     # keys after the query's position
+                    Ob, Lb = _softmax_rows(S, v_s[: kend - a])
+                    return idx, Ob.reshape(len(idx), G, D), Lb.reshape(len(idx), G)
 
-            batches = [idx_s[i:i + batch] for i in range(0, len(idx_s), batch)]
-            with ThreadPoolExecutor(max_workers=threads) as ex:
+                # longest batches first, so the pool's threads finish together
+                batches = [idx_s[i:i + batch] for i in range(0, len(idx_s), batch)][::-1]
                 for idx, Ob, Lb in ex.map(work, batches):
                     for gi, h in enumerate(heads):
                         O[idx, h, :] = Ob[:, gi, :]

@@ -1,7 +1,13 @@
 import os
 import sys
 
-import pytest
+# The fp64 oracle runs its matrix products on a thread pool, one product per
+# thread: BLAS itself stays single-threaded so that the pool's threads do not
+# oversubscribe the cores (set before numpy is first imported).
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import pytest  # noqa: E402
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
