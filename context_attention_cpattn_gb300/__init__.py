@@ -86,6 +86,7 @@ _SIGNATURES = {
     "cpattn_dcp_schedule": [_P, _I64, _P, _I32, _P, _P, _P, _P, _P],
     "cpattn_dcp_sweep": [_P, _I64, _P, _I32, _I32, _I32, _I32, _P, _P, _P],
     "cpattn_sync_status": [_P, _P],
+    "cpattn_static_sync_status": [_P],
     "cpattn_last_error_string": [],
     "cpattn_version": [],
 }
@@ -372,6 +373,11 @@ def cpattn_fwd_flops(cu_seqlens, H: int, D: int, causal: bool) -> int:
 
 def cpattn_sync_status(workspace=None, stream=None):
     _check(lib().cpattn_sync_status(_ptr(workspace), _stream(stream)))
+
+
+def cpattn_static_sync_status(stream=None):
+    """Fault word of cpattn_fwd_static's static array on the current device."""
+    _check(lib().cpattn_static_sync_status(_stream(stream)))
 
 
 # ------------------------------------------------------ Dynamic-CP scheduler

@@ -12,7 +12,9 @@
 // the library, held until the process exits.  Host code cannot use the
 // array's name as a device address, so the first call on each device looks
 // the address up with cudaGetSymbolAddress (with that device current) and
-// caches it.
+// caches it.  A kernel that gives up on a bounded wait records the fault in
+// the array's header; cpattn_static_sync_status reads it back (again without
+// allocating).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -131,5 +133,22 @@ extern "C" cpattn_status_t cpattn_fwd_static(const cpattn_plan_t* cplan, const v
     if (!err.empty()) return set_error(CPATTN_INVALID_ARG, err);
     return set_error(CPATTN_CUDA_ERROR, std::string("attention kernel launch: ") + cudaGetErrorString(e));
   }
+  return CPATTN_OK;
+}
+
+extern "C" cpattn_status_t cpattn_static_sync_status(void* stream_ptr) {
+  using cpattn::set_error;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return set_error(CPATTN_CUDA_ERROR, std::string("stream synchronize: ") + cudaGetErrorString(e));
+  // The header of the current device's array, copied by symbol into host stack memory.
+  cpattn::WsHeader h;
+  e = cudaMemcpyFromSymbol(&h, g_cpattn_static_scratch, sizeof(h), 0, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess)
+    return set_error(CPATTN_CUDA_ERROR, std::string("reading the static scratch fault word: ") + cudaGetErrorString(e));
+  if (h.fault != 0)
+    return set_error(CPATTN_DEVICE_FAULT, "kernel fault " + std::to_string(h.fault) + " in block " +
+                                              std::to_string(h.info) + " at " + std::to_string(h.detail) +
+                                              " (static scratch)");
   return CPATTN_OK;
 }

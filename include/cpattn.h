@@ -392,13 +392,23 @@ cpattn_status_t cpattn_scatter_rows(const void* src, void* dst, int64_t dst_rows
  *   The work list is copied from pageable host memory, so the call waits for
  *   work already queued on `stream` before it returns.
  *   Errors: CPATTN_WORKSPACE when the plan's work list does not fit in the
- *   array (the message gives both sizes); CPATTN_UNSUPPORTED for GRID2D plans,
- *   whose shard gather needs more scratch than the array holds.  A fault that
- *   a kernel records in the array's fault word is not reported by
- *   cpattn_sync_status. */
+ *   array (the message gives both sizes); CPATTN_UNSUPPORTED for GRID2D,
+ *   ULYSSES2D and PAIRED plans, whose shard gathers and all-to-all buffers
+ *   need more scratch than the array holds.  A bounded wait that runs out
+ *   inside the kernel records a fault in the array's header (the output is
+ *   then incomplete); cpattn_static_sync_status reports it. */
 cpattn_status_t cpattn_fwd_static(const cpattn_plan_t* plan, const void* q, const void* k, const void* v,
                                   cpattn_dtype_t dtype, int32_t H, int32_t Hkv, int32_t D, float scale,
                                   int32_t causal, void* o, float* lse, void* stream);
+
+/* Synchronise `stream`, then report a fault that a cpattn_fwd_static kernel
+ * recorded in the static array of the current device (CPATTN_DEVICE_FAULT,
+ * with the block and the wait in the message) or a CUDA error
+ * (CPATTN_CUDA_ERROR).  Allocates nothing: the header is copied by symbol
+ * into host stack memory.  The next cpattn_fwd_static call on the device
+ * clears the fault word.  Like the array, the word is shared by every call:
+ * check it before the next call is issued. */
+cpattn_status_t cpattn_static_sync_status(void* stream);
 
 /* --------------------------------------------------------------- loss, FLOPs */
 
