@@ -48,9 +48,8 @@ UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "dynamic_cp_microbatch"
 FALLBACK_BF16_TFLOPS = 1900.0
 TC_SOURCES = ("context_attention_cpattn_gb300/csrc/attn_tc.cu", "context_attention_cpattn_gb300/csrc/common.cuh")
-TRAFFIC_FILE = "profiles/attn_fwd_tc_dynamic_cp_microbatch.md"
+TRAFFIC_FILE = "profiles/traffic.json"
 BWD_SOURCES = ("context_attention_cpattn_gb300/csrc/attn_bwd_tc.cu", "context_attention_cpattn_gb300/csrc/common.cuh")
-BWD_TRAFFIC_FILE = "profiles/attn_bwd_tc_dynamic_cp_microbatch.md"
 
 
 def parse_args(argv=None):
@@ -63,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the CPU oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the long-sequence workloads after the headline one")
     ap.add_argument("--aux", action="store_true",
                     help="time the HBM-bound kernels (merge, shard gather, loss norm) instead of the forward")
     ap.add_argument("--mesh", default="",
@@ -122,37 +123,127 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+# NVML clock-event reason bits (read-only queries; nothing is ever set)
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
 
 def clock_csv_path(tag: str) -> str:
     """Where the raw clock samples go: the directory in CPATTN_CLOCKS_DIR, else /tmp."""
     return os.path.join(os.environ.get("CPATTN_CLOCKS_DIR", "/tmp"), f"cpattn_clocks_{tag}.csv")
 
 
+def nvml_index(local_rank: int) -> int:
+    """NVML index of the GPU this process uses: CUDA_VISIBLE_DEVICES maps the
+    CUDA ordinal to the physical one when it lists plain indices."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x.strip() for x in vis.split(",") if x.strip()]
+    if ids and all(x.isdigit() for x in ids) and local_rank < len(ids):
+        return int(ids[local_rank])
+    return local_rank
+
+
+class _Nvml:
+    """The few read-only NVML queries the sampler needs, through ctypes."""
+
+    def __init__(self, index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+
+    def sample(self):
+        c = self.c
+        mhz, mw, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz))          # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(mw))
+        self.reasons_fn(self.h, c.byref(rs))
+        return float(mhz.value), mw.value / 1e3, int(rs.value)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """SM clock, power and throttle reasons sampled every 10 ms from a host
+    thread (NVML, read-only), or by nvidia-smi every 200 ms where NVML cannot
+    be loaded.  ``mark()`` brackets a region; ``summary(region)`` gives the
+    median SM clock under load and the reasons seen in it."""
 
-    def __init__(self, gpu_index: int, path: str):
-        self.path = path
+    def __init__(self, local_rank: int, path: str, period_s: float = 0.01):
+        import threading
+        self.samples = []   # (host time, sm MHz, max MHz, power W, reasons set)
+        self.marks = {}
         self.proc = None
+        self.nvml = None
+        self.path = path
         try:
-            self.f = open(path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
-                 "-i", str(gpu_index)], stdout=self.f, stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            self.nvml = _Nvml(nvml_index(local_rank))
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            self.stop_ev = threading.Event()
 
-    def stop(self) -> dict | None:
-        if self.proc is None:
+            def loop():
+                while not self.stop_ev.is_set():
+                    mhz, w, rs = self.nvml.sample()
+                    self.samples.append((time.perf_counter(), mhz, self.nvml.max_mhz, w,
+                                         {n for bit, n in _NVML_REASONS.items() if rs & bit}))
+                    time.sleep(period_s)
+
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+        else:
+            try:
+                self.f = open(path, "w")
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                     "-i", str(nvml_index(local_rank))], stdout=self.f, stderr=subprocess.DEVNULL)
+            except (OSError, FileNotFoundError):
+                self.proc = None
+
+    def mark(self, name: str):
+        self.marks[name] = time.perf_counter()
+
+    def stop(self):
+        if self.nvml is not None:
+            time.sleep(0.02)
+            self.stop_ev.set()
+            self.thread.join(timeout=2)
+            self.nvml.close()
+        elif self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, start: str | None = None, end: str | None = None) -> dict | None:
+        if self.nvml is None:
+            if self.proc is None:
+                return None
+            return summarise_clocks(open(self.path).read())
+        t0 = self.marks.get(start, -1e30) if start else -1e30
+        t1 = self.marks.get(end, 1e30) if end else 1e30
+        sel = [x for x in self.samples if t0 <= x[0] <= t1]
+        if not sel:
             return None
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.f.close()
-        return summarise_clocks(open(self.path).read())
+        sm = [x[1] for x in sel]
+        top = max(sm)
+        loaded = [v for v in sm if v >= 0.5 * top] or sm
+        reasons = sorted(set().union(*(x[4] for x in sel)))
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(x[2] for x in sel), "samples": len(sel),
+                "power_w_max": max(x[3] for x in sel), "reasons": reasons, "source": "nvml 10 ms"}
 
 
 def summarise_clocks(text: str) -> dict | None:
@@ -175,7 +266,7 @@ def summarise_clocks(text: str) -> dict | None:
     top = max(sm)
     loaded = [s for s in sm if s >= 0.5 * top] or sm
     return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "samples": len(sm),
-            "reasons": sorted(reasons)}
+            "reasons": sorted(reasons), "source": "nvidia-smi 200 ms"}
 
 
 # ------------------------------------------------------------------ peaks, traffic
@@ -197,20 +288,17 @@ def tc_source_hash(sources=TC_SOURCES) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, path=TRAFFIC_FILE, sources=TC_SOURCES):
-    """DRAM bytes per launch of a kernel from its committed ncu summary, if
-    the summary was taken on the current kernel source and this workload."""
-    path = os.path.join(ROOT, path)
-    if workload != DEFAULT_WORKLOAD or not os.path.exists(path):
+def recorded_traffic(workload: str, kernel: str = "attn_fwd_tc_kernel", sources=TC_SOURCES):
+    """DRAM bytes per launch of a kernel from profiles/traffic.json, if they
+    were taken on the current kernel source and this workload."""
+    try:
+        with open(os.path.join(ROOT, TRAFFIC_FILE)) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
         return None
-    vals = {}
-    for line in open(path):
-        if line.startswith("traffic_bytes_per_launch=") or line.startswith("source_sha256="):
-            k, v = line.strip().split("=", 1)
-            vals[k] = v
-    if vals.get("source_sha256") != tc_source_hash(sources) or "traffic_bytes_per_launch" not in vals:
+    if not rec or rec.get("workload") != workload or rec.get("source_sha256") != tc_source_hash(sources):
         return None
-    return float(vals["traffic_bytes_per_launch"])
+    return float(rec["dram_bytes_per_launch"])
 
 
 # ------------------------------------------------------------------ CPU oracle legs
@@ -351,22 +439,26 @@ def run_ours(args, rep: Replicas):
             ev1.record(stream)
         cp.cpattn_token_loss_norm(loss_d, valid_d, out_loss, out_cnt, stream=stream)
 
+    sampler = ClockSampler(rep.local, clock_csv_path(f"rank{rep.rank}"))
+    sampler.mark("warmup")
     for _ in range(args.warmup):
         step()
     cp.cpattn_sync_status(ws, stream)
 
-    sampler = ClockSampler(rep.local, clock_csv_path(f"rank{rep.rank}"))
     fwd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     rep.barrier()
     torch.cuda.synchronize(dev)
+    sampler.mark("timed")
     start.record(stream)
     for i in range(args.steps):
         step(*fwd_ev[i])
     end.record(stream)
     torch.cuda.synchronize(dev)
+    sampler.mark("timed_end")
     rep.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.summary("timed", "timed_end")
+    clocks_run = sampler.summary("warmup", "timed_end")
     cp.cpattn_sync_status(ws, stream)
     elapsed = start.elapsed_time(end) / 1e3
     fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
@@ -451,6 +543,17 @@ def run_ours(args, rep: Replicas):
         if not torch.equal(sets[(args.warmup + args.steps - 1) % 2]["o_h"].to(dev), o):
             raise RuntimeError("end-to-end output differs from the device-resident run")
 
+    per_config = backward = None
+    if rep.world == 1 and not args.no_per_config and not args.mesh and args.workload == DEFAULT_WORKLOAD:
+        backward = time_backward(cp, w, qd, kd, vd, dev, stream, sampler, max(args.steps, 3), max(args.warmup, 3),
+                                 tag="bwd_" + w.name)
+        del qd, kd, vd, o, lse, ws
+        if e2e is not None:
+            del sets
+        torch.cuda.empty_cache()
+        per_config = {name: time_config(cp, name, n, dev, stream, sampler) for name, n in PER_CONFIG}
+    sampler.stop()
+
     if rep.rank != 0:
         return
     peak, peak_src = measured_peak()
@@ -470,16 +573,86 @@ def run_ours(args, rep: Replicas):
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
+        "clocks_warmup_and_timed": clocks_run,
         "plan_ms": plan_ms,
         "fwd_ms_mean": 1e3 * fwd_mean_s,
         "fwd_ms_min": min(fwd_ms),
         "tc_source_sha256": tc_source_hash(),
         "mma_area_useful": useful_mma_fraction(plan, w.causal, w.dtype),
     }
+    if per_config is not None:
+        line["per_config"] = per_config
+    if backward is not None:
+        line["backward"] = backward
     if not args.no_cpu_baseline and rep.world == 1 and w.mode != "paired":
         # (the CPU legs evaluate the causal / bidirectional oracle; paired plans use another mask)
         line["cpu_baseline"] = run_cpu_baseline(args)
     print(json.dumps(line), flush=True)
+
+
+# The other full-size workloads, timed in the same process after the headline
+# one: (name, timed steps).  Three warm-up calls each; inputs larger than L2.
+PER_CONFIG = (("long_video_200k_gqa", 5), ("video_latent_grid2d", 20), ("single_seq_1m_gqa", 2))
+
+
+def measured_sustained() -> float | None:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def time_config(cp, name, steps, dev, stream, sampler, warmup=3):
+    """cpattn_fwd on one workload: TFLOP/s of valid-token FLOPs over `steps`
+    calls timed by CUDA events on the launching stream."""
+    import torch
+
+    import inputs
+    w = inputs.workload(name)
+    q_h, k_h, v_h = inputs.make_qkv(w)
+    qd, kd, vd = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    del q_h, k_h, v_h
+    plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
+    flops = cp.cpattn_fwd_flops(w.cu_seqlens, w.H, w.D, w.causal)
+    ws = torch.empty(cp.cpattn_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal), dtype=torch.uint8,
+                     device=dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.H, w.T), dtype=torch.float32, device=dev)
+
+    def call():
+        cp.cpattn_fwd(plan, qd, kd, vd, o, lse, ws, scale=w.scale, causal=w.causal, stream=stream)
+
+    for _ in range(warmup):
+        call()
+    cp.cpattn_sync_status(ws, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    sampler.mark(name)
+    for a, b in ev:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark(name + "_end")
+    cp.cpattn_sync_status(ws, stream)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    mean_s = statistics.fmean(ms) / 1e3
+    value = flops / mean_s / 1e12
+    peak, src = measured_peak()
+    out = {"value": value, "unit": UNIT, "frac": value / peak, "peak": peak, "peak_source": src,
+           "ms_per_step": 1e3 * mean_s, "ms_min": min(ms), "steps": steps, "warmup": warmup,
+           "flops_per_step": flops, "T": w.T, "H": w.H, "Hkv": w.Hkv, "mode": w.mode, "cp": w.cp,
+           "causal": w.causal, "clocks": sampler.summary(name, name + "_end"),
+           "mma_area_useful": useful_mma_fraction(plan, w.causal, w.dtype),
+           "l2": "inputs larger than L2"}
+    sustained = measured_sustained()
+    if sustained and mean_s > 1.0:
+        out["frac_of_sustained"] = value / sustained
+        out["peak_sustained"] = sustained
+    del qd, kd, vd, o, lse, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 # Kernel tile shapes (rows per tile, keys or queries per piece) of the bf16 and
@@ -501,11 +674,62 @@ def useful_mma_fraction(plan, causal: bool, dtype: str = "bf16", backward: bool 
     return groups * plan.allowed_pairs(causal) / executed if executed else None
 
 
+def time_backward(cp, w, qd, kd, vd, dev, stream, sampler, steps, warmup, tag="bwd"):
+    """cpattn_bwd (delta/LSE prep, the tensor-core kernel, dQ conversion) on
+    one workload, timed per call with CUDA events on its stream.  FLOPs = 2.5 x
+    the forward's (five products of the forward's shape where the forward has
+    two), over valid (causal) pairs only.  Returns the result as a dict."""
+    import torch
+
+    import inputs
+    dod = inputs.make_dout(w).to(dev)
+    plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
+    fwd_flops = cp.cpattn_fwd_flops(w.cu_seqlens, w.H, w.D, w.causal)
+    flops = fwd_flops * 5 // 2
+    ws = torch.empty(max(cp.cpattn_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal),
+                         cp.cpattn_bwd_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal)),
+                     dtype=torch.uint8, device=dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.H, w.T), dtype=torch.float32, device=dev)
+    cp.cpattn_fwd(plan, qd, kd, vd, o, lse, ws, scale=w.scale, causal=w.causal, stream=stream)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+
+    def step():
+        cp.cpattn_bwd(plan, qd, kd, vd, o, lse, dod, dq, dk, dv, ws, scale=w.scale, causal=w.causal, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    cp.cpattn_sync_status(ws, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    sampler.mark(tag)
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.mark(tag + "_end")
+    cp.cpattn_sync_status(ws, stream)
+    ms = [a.elapsed_time(b) for a, b in ev]
+    mean_s = statistics.fmean(ms) / 1e3
+    peak, peak_src = measured_peak()
+    achieved = flops / mean_s / 1e12
+    launches = 3 + (4 if w.mode == "grid2d" else 0)
+    return {
+        "metric": "packed varlen attention bwd TFLOP/s (valid tokens, 2.5x forward FLOPs)", "value": achieved,
+        "unit": UNIT, "steps": steps, "warmup": warmup, "ms_per_step": 1e3 * mean_s,
+        "ms_min": min(ms), "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": config_of(w, flops),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "peak_source": peak_src,
+                     "traffic": recorded_traffic(w.name, "attn_bwd_tc_kernel", BWD_SOURCES),
+                     "kernel": "cpattn_bwd call (pre + attn_bwd_tc_kernel + post), CUDA events per call"},
+        "gpu_launches": launches * steps, "clocks": sampler.summary(tag, tag + "_end"),
+        "mma_area_useful": useful_mma_fraction(plan, w.causal, w.dtype, backward=True)}
+
+
 def run_bwd(args):
-    """Backward on the workload: cpattn_bwd (delta/LSE prep, the tensor-core
-    kernel, dQ conversion) timed per call with CUDA events on its stream.
-    FLOPs = 2.5 x the forward's (five products of the forward's shape where
-    the forward has two), over valid (causal) pairs only."""
+    """Backward on the workload (see time_backward), printed as one JSON line."""
     import torch
 
     import context_attention_cpattn_gb300 as cp
@@ -516,51 +740,10 @@ def run_bwd(args):
     w = inputs.workload(args.workload)
     q_h, k_h, v_h = inputs.make_qkv(w)
     qd, kd, vd = q_h.to(dev), k_h.to(dev), v_h.to(dev)
-    dod = inputs.make_dout(w).to(dev)
-    plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
-    fwd_flops = cp.cpattn_fwd_flops(w.cu_seqlens, w.H, w.D, w.causal)
-    flops = fwd_flops * 5 // 2
-    ws = torch.empty(max(cp.cpattn_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal),
-                         cp.cpattn_bwd_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal)),
-                     dtype=torch.uint8, device=dev)
-    o = torch.empty_like(qd)
-    lse = torch.empty((w.H, w.T), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    cp.cpattn_fwd(plan, qd, kd, vd, o, lse, ws, scale=w.scale, causal=w.causal, stream=stream)
-    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-
-    def step():
-        cp.cpattn_bwd(plan, qd, kd, vd, o, lse, dod, dq, dk, dv, ws, scale=w.scale, causal=w.causal, stream=stream)
-
-    for _ in range(args.warmup):
-        step()
-    cp.cpattn_sync_status(ws, stream)
     sampler = ClockSampler(0, clock_csv_path("bwd"))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    torch.cuda.synchronize(dev)
-    for a, b in ev:
-        a.record(stream)
-        step()
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks = sampler.stop()
-    cp.cpattn_sync_status(ws, stream)
-    ms = [a.elapsed_time(b) for a, b in ev]
-    mean_s = statistics.fmean(ms) / 1e3
-    peak, peak_src = measured_peak()
-    achieved = flops / mean_s / 1e12
-    launches = 3 + (4 if w.mode == "grid2d" else 0)
-    print(json.dumps({
-        "metric": "packed varlen attention bwd TFLOP/s (valid tokens, 2.5x forward FLOPs)", "value": achieved,
-        "unit": UNIT, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean_s,
-        "ms_min": min(ms), "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": config_of(w, flops),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
-                     "peak_source": peak_src,
-                     "traffic": recorded_traffic(w.name, BWD_TRAFFIC_FILE, BWD_SOURCES),
-                     "kernel": "cpattn_bwd call (pre + attn_bwd_tc_kernel + post), CUDA events per call"},
-        "gpu_launches": launches * args.steps, "clocks": clocks,
-        "mma_area_useful": useful_mma_fraction(plan, w.causal, w.dtype, backward=True)}), flush=True)
+    line = time_backward(cp, w, qd, kd, vd, dev, torch.cuda.current_stream(dev), sampler, args.steps, args.warmup)
+    sampler.stop()
+    print(json.dumps(line), flush=True)
 
 
 def measured_hbm() -> tuple[float, str]:
