@@ -173,12 +173,12 @@ class _Nvml:
 
 
 class ClockSampler:
-    """SM clock, power and throttle reasons sampled every 10 ms from a host
+    """SM clock, power and throttle reasons sampled every 2 ms from a host
     thread (NVML, read-only), or by nvidia-smi every 200 ms where NVML cannot
     be loaded.  ``mark()`` brackets a region; ``summary(region)`` gives the
     median SM clock under load and the reasons seen in it."""
 
-    def __init__(self, local_rank: int, path: str, period_s: float = 0.01):
+    def __init__(self, local_rank: int, path: str, period_s: float = 0.002):
         import threading
         self.samples = []   # (host time, sm MHz, max MHz, power W, reasons set)
         self.marks = {}
@@ -197,7 +197,7 @@ class ClockSampler:
                     mhz, w, rs = self.nvml.sample()
                     self.samples.append((time.perf_counter(), mhz, self.nvml.max_mhz, w,
                                          {n for bit, n in _NVML_REASONS.items() if rs & bit}))
-                    time.sleep(period_s)
+                    self.stop_ev.wait(period_s)
 
             self.thread = threading.Thread(target=loop, daemon=True)
             self.thread.start()
@@ -243,7 +243,7 @@ class ClockSampler:
         loaded = [v for v in sm if v >= 0.5 * top] or sm
         reasons = sorted(set().union(*(x[4] for x in sel)))
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(x[2] for x in sel), "samples": len(sel),
-                "power_w_max": max(x[3] for x in sel), "reasons": reasons, "source": "nvml 10 ms"}
+                "power_w_max": max(x[3] for x in sel), "reasons": reasons, "source": "nvml, 2 ms period"}
 
 
 def summarise_clocks(text: str) -> dict | None:
@@ -655,8 +655,8 @@ def time_config(cp, name, steps, dev, stream, sampler, warmup=3):
     return out
 
 
-# Kernel tile shapes (rows per tile, keys or queries per piece) of the bf16 and
-# fp32 forward and backward kernels.
+# Kernel tile shapes (rows per tile, keys or queries per kernel tile) of the
+# bf16 and fp32 forward and backward kernels.
 TILE_SHAPES = {(False, "bf16"): (128, 64), (False, "fp32"): (64, 32),
                (True, "bf16"): (128, 64), (True, "fp32"): (32, 64)}
 

@@ -87,6 +87,7 @@ _SIGNATURES = {
     "cpattn_dcp_sweep": [_P, _I64, _P, _I32, _I32, _I32, _I32, _P, _P, _P],
     "cpattn_sync_status": [_P, _P],
     "cpattn_static_sync_status": [_P],
+    "cpattn_debug_wait_fault": [ctypes.c_uint32, _I32],
     "cpattn_last_error_string": [],
     "cpattn_version": [],
 }
@@ -373,6 +374,12 @@ def cpattn_fwd_flops(cu_seqlens, H: int, D: int, causal: bool) -> int:
 
 def cpattn_sync_status(workspace=None, stream=None):
     _check(lib().cpattn_sync_status(_ptr(workspace), _stream(stream)))
+
+
+def cpattn_debug_wait_fault(wait_limit_us: int, withhold_first_v: bool = False):
+    """Fault-path test support: a short limit on every bounded kernel wait and,
+    optionally, a withheld V load in the bf16 forward (see the C header)."""
+    _check(lib().cpattn_debug_wait_fault(int(wait_limit_us), int(bool(withhold_first_v))))
 
 
 def cpattn_static_sync_status(stream=None):

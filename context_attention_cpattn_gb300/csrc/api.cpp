@@ -2,7 +2,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
+#include <cstddef>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -21,6 +23,11 @@ using cpattn::WsHeader;
 namespace {
 
 thread_local std::string g_err;
+
+// Fault-path test settings (cpattn_debug_wait_fault), written into every
+// workspace header a call uploads.  Zero: off.
+std::atomic<uint32_t> g_test_wait_limit_us{0};
+std::atomic<uint32_t> g_test_withhold{0};
 
 cpattn_status_t fail(cpattn_status_t s, const std::string& msg) {
   g_err = msg;
@@ -142,6 +149,13 @@ cpattn_status_t upload_worklist(const cpattn_plan_t* plan, const WorkList& wl, c
   }
   cudaError_t e = cudaMemsetAsync(ws, 0, CPATTN_WS_HEADER_BYTES, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync (fault word)");
+  const uint32_t test_fields[2] = {g_test_wait_limit_us.load(), g_test_withhold.load()};
+  if (test_fields[0] || test_fields[1]) {
+    // pageable source: the copy is staged before the call returns
+    e = cudaMemcpyAsync(ws + offsetof(WsHeader, wait_limit_us), test_fields, sizeof(test_fields),
+                        cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (fault-path test settings)");
+  }
   if (pt.ptr) {
     e = cudaMemcpyAsync(ws + L.tiles, pt.ptr, pt.bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync (work list)");
@@ -841,6 +855,15 @@ cpattn_status_t cpattn_fwd_flops(const int32_t* cu, int32_t n_seqs, int32_t H, i
   if (f > (unsigned __int128)UINT64_MAX) return fail(CPATTN_INVALID_ARG, "FLOP count overflows uint64");
   if (out_u64) *out_u64 = (uint64_t)f;
   if (out_f64) *out_f64 = (double)(uint64_t)f;
+  return CPATTN_OK;
+}
+
+cpattn_status_t cpattn_debug_wait_fault(uint32_t wait_limit_us, int32_t withhold_first_v) {
+  if (withhold_first_v != 0 && wait_limit_us == 0)
+    return fail(CPATTN_INVALID_ARG, "withholding a load needs a short wait limit (wait_limit_us > 0)");
+  if (wait_limit_us > 10000000u) return fail(CPATTN_INVALID_ARG, "wait_limit_us must be at most 10 s");
+  g_test_wait_limit_us.store(wait_limit_us);
+  g_test_withhold.store(withhold_first_v != 0 ? 1u : 0u);
   return CPATTN_OK;
 }
 

@@ -14,31 +14,31 @@
 // index, the rest from an atomic counter, longest first) through a ring of
 // shared-memory slots.
 //
-// Warp roles (320 threads):
+// Warp roles (224 threads):
 //   warp 0      TMA producer: Q per item, then K and V through two-deep
 //               rings in the order the MMAs read them (K_0, K_1, V_0, K_2,
 //               V_1, ...); K_j is refilled once S_j has read it, V_j once
 //               PV_j has.
-//   warp 1      TMEM allocator and MMA issuer (one thread).  TMEM holds two S
-//               buffers of 64 columns and O (128 columns).  Order per item:
-//                 S_0, S_1, PV_0, S_2, PV_1, S_3, ...
+//   warp 1      TMEM allocator and S issuer (one thread).  TMEM holds two S
+//               buffers of 64 columns and O (128 columns).
 //                 S_j  = Q K_j^T  (M=128, N=64, K=D)   A, B from shared memory
+//               S_j goes into buffer j & 1 once PV_{j-2} has read the P that
+//               buffer held.
+//   warp 2      PV issuer (one thread):
 //                 O   += P_j V_j  (M=128, N=D,  K=64)  A = P_j from TMEM, B = V_j
-//               so the scores of the next tile are computed while the softmax
-//               warps work on this one.  P_j is written over the first 32
-//               columns of S_j's buffer; S_{j+2} reuses that buffer after PV_j
-//               (tcgen05.mma ops from one thread run in issue order).
-//   warps 2-5   softmax, one query row per thread: read S_j from TMEM, apply
-//               the causal / run-end mask from token positions, update the
-//               running max and sum, write P (bf16 pairs) back to TMEM, and
-//               rescale O when the running max grows by more than 2^8
-//               (otherwise the stale max is kept: O and the sum share it, so
-//               the final O/l is exact).  A rescale first waits for PV_{j-1}.
-//               At the end of an item the row's max and sum go to shared
-//               memory and the warps move on to the next item at once.
-//   warps 6-9   epilogue, one query row per thread: once the item's last PV
-//               has run, read O from TMEM, release it for the next item's
-//               first PV, and write O/l and the LSE at the output rows.
+//               A tcgen05.mma costs its issuing thread about a hundred cycles
+//               whatever its shape, so the two products of a tile issue from
+//               two threads, ordered by mbarriers (S_j after PV_{j-2}, PV_j
+//               after the softmax of tile j), not by one thread's issue order.
+//   warps 3-6   softmax and epilogue, one query row per thread: read S_j from
+//               TMEM, apply the causal / run-end mask from token positions,
+//               update the running max and sum, write P (bf16 pairs) back over
+//               the first 32 columns of S_j's buffer, and rescale O when the
+//               running max grows by more than 2^8 (otherwise the stale max is
+//               kept: O and the sum share it, so the final O/l is exact).  A
+//               rescale first waits for PV_{j-1}.  After an item's last PV they
+//               read O, release it for the next item's first PV, and write O/l
+//               and the LSE at the output rows.
 //
 // Shared-memory operand layouts (1024-byte aligned, SWIZZLE_128B):
 //   Q:    [128 rows][64 columns] boxes, K-major.
@@ -86,9 +86,8 @@ struct TcCfg {
   static constexpr uint32_t OFF_K = Q_BYTES;          // K[2]
   static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;  // V[2]
   static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // 27 mbarriers (216 bytes) fit below
-  static constexpr uint32_t OFF_STATS = OFF_MISC + 64;  // [2 items][128 rows] (max, sum)
-  static constexpr uint32_t SMEM = OFF_STATS + 2 * 128 * 8 + 1024;  // + alignment slack
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // 29 mbarriers (232 bytes) fit below
+  static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 256;              // S0 | S1 | O
   static constexpr uint32_t TM_S = 0, TM_O = 128;         // S buffer b at TM_S + 64 b
 };
@@ -132,7 +131,7 @@ __device__ __forceinline__ Item item_of(int i, int n_tiles, int G) {
 }
 
 template <int D, bool kPartial>
-__global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<D>;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 64, false, false);
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
@@ -152,19 +151,22 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
   uint64_t* o_done = bars + 14;    // after every PV
   uint64_t* o_final = bars + 15;   // after an item's last PV
   uint64_t* o_free = bars + 16;    // the epilogue has read O
-  uint64_t* drain = bars + 17;
+  uint64_t* drain = bars + 17;     // the S issuer's MMAs have landed
   uint64_t* item_full = bars + 18;   // [4] ring of work items handed from the producer
   uint64_t* item_empty = bars + 22;  // [4]
-  uint64_t* stats_full = bars + 26;  // the softmax warps have left an item's row max and sum
+  uint64_t* s_free = bars + 26;      // [2] PV_j has read P_j: the buffer may take S_{j+2}
+  uint64_t* drain2 = bars + 28;      // the PV issuer's MMAs have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);     // loads issued: [0] K, [1] V, [2] Q
   int* item_ring = reinterpret_cast<int*>(smem + C::OFF_MISC + 32);  // [4]
-  float2* stats = reinterpret_cast<float2*>(smem + C::OFF_STATS);     // [2][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.H / p.Hkv;
   const int n_items = p.n_tiles * p.H;
+  // every bounded wait gives up after 4 s, or after the workspace's shorter
+  // limit when a fault-path test set one
+  const uint64_t wait_ns = p.ws->wait_limit_us ? (uint64_t)p.ws->wait_limit_us * 1000ull : kWaitLimitNs;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -176,15 +178,16 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
       mbar_init(v_empty + b, 1);
       mbar_init(s_full + b, 1);
       mbar_init(p_full + b, 128);
+      mbar_init(s_free + b, 1);
     }
     mbar_init(o_done, 1);
     mbar_init(o_final, 1);
     mbar_init(o_free, 128);
     mbar_init(drain, 1);
-    mbar_init(stats_full, 128);
+    mbar_init(drain2, 1);
     for (int r = 0; r < 4; ++r) {
       mbar_init(item_full + r, 1);
-      mbar_init(item_empty + r, 257);  // the MMA thread, 128 softmax and 128 epilogue threads
+      mbar_init(item_empty + r, 130);  // the two MMA threads and the 128 softmax threads
     }
     *abort_flag = 0;
     issued[0] = issued[1] = issued[2] = 0;
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
   // counted across items (g), so double-buffered barriers keep alternating
   // phases from one item to the next: buffer g & 1, phase parity (g >> 1) & 1.
   auto take_item = [&](int k, uint32_t where) -> int {  // consumers: item k of this block, or -1
-    if (!wait_bounded(item_full + (k & 3), (k >> 2) & 1, abort_flag, p.ws, where)) return -2;
+    if (!wait_bounded(item_full + (k & 3), (k >> 2) & 1, abort_flag, p.ws, where, wait_ns)) return -2;
     const int i = item_ring[k & 3];
     mbar_arrive(item_empty + (k & 3));
     return i;
@@ -216,11 +219,14 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
+      // fault-path test support: block 0 never loads its first V tile, so the
+      // PV issuer's bounded wait for it runs out
+      const bool withhold_v0 = (blockIdx.x == 0) && (p.ws->withhold == 1u);
       int g = 0, qc = 0;
       bool ok = true;
       int i = blockIdx.x;
       for (int k = 0; ok; ++k) {
-        if (k >= 4 && !wait_bounded(item_empty + (k & 3), ((k >> 2) - 1) & 1, abort_flag, p.ws, 1)) break;
+        if (k >= 4 && !wait_bounded(item_empty + (k & 3), ((k >> 2) - 1) & 1, abort_flag, p.ws, 1, wait_ns)) break;
         item_ring[k & 3] = (i < n_items) ? i : -1;
         mbar_arrive(item_full + (k & 3));
         if (i >= n_items) break;
@@ -229,7 +235,7 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
         i = (int)gridDim.x + (int)atomicAdd(&p.ws->next_item, 1u);
         if (tile.n_kv_tiles == 0) continue;
         // Q of this item once every S MMA of the previous item has read its Q
-        if (qc > 0 && !wait_bounded(q_empty, (qc - 1) & 1, abort_flag, p.ws, 2)) break;
+        if (qc > 0 && !wait_bounded(q_empty, (qc - 1) & 1, abort_flag, p.ws, 2, wait_ns)) break;
         mbar_arrive_expect_tx(q_full, C::Q_BYTES);
         for (int kb = 0; kb < C::KB; ++kb)
           tma_load_3d(smem + kb * C::QBOX, &p.tm_q, q_full, kb * 64, it.h, tile.q_row0);
@@ -240,7 +246,7 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
         PieceCursor c{tile.run_begin, 0, tile.run_end};
         auto load_k = [&](int gk, int row) -> bool {
           const int b = gk & 1;
-          if (gk >= 2 && !wait_bounded(k_empty + b, ((gk >> 1) - 1) & 1, abort_flag, p.ws, 3)) return false;
+          if (gk >= 2 && !wait_bounded(k_empty + b, ((gk >> 1) - 1) & 1, abort_flag, p.ws, 3, wait_ns)) return false;
           mbar_arrive_expect_tx(k_full + b, C::KV_BYTES);
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(smem + C::OFF_K + b * C::KV_BYTES + kb * C::KVBOX, &p.tm_k, k_full + b, kb * 64, it.g, row);
@@ -256,7 +262,8 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
             row_next = c.next(p.runs).row0;
             if (!load_k(g + 1, row_next)) { ok = false; break; }
           }
-          if (g >= 2 && !wait_bounded(v_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 4)) { ok = false; break; }
+          if (g >= 2 && !wait_bounded(v_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 4, wait_ns)) { ok = false; break; }
+          if (withhold_v0 && g == 0) continue;
           mbar_arrive_expect_tx(v_full + b, C::KV_BYTES);
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(smem + C::OFF_V + b * C::KV_BYTES + kb * C::KVBOX, &p.tm_v, v_full + b, kb * 64, it.g, row);
@@ -265,47 +272,59 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      // S_g = Q K_g^T into S buffer g & 1
-      auto issue_s = [&](int gg) {
-        const uint32_t kbase = sK + (gg & 1) * C::KV_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qoff = (kk >> 2) * C::QBOX + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * C::KVBOX + (kk & 3) * 32;
-          umma_bf16_ss(tmem + C::TM_S + 64u * (gg & 1), smem_desc_sw128(sQ + qoff, 16, 1024),
-                       smem_desc_sw128(kbase + koff, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-        }
-      };
-      int g = 0, qc = 0, oc = 0;
+      const uint32_t sQ = smem_u32(smem), sK = smem_u32(smem + C::OFF_K);
+      int g = 0, qc = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int i = take_item(k, 5);
         if (i < 0) break;
         const int n_kv = p.tiles[item_of(i, p.n_tiles, G).tile_id].n_kv_tiles;
         if (n_kv == 0) continue;
-        ok = wait_bounded(q_full, qc & 1, abort_flag, p.ws, 6);
-        if (!ok) break;
+        if (!wait_bounded(q_full, qc & 1, abort_flag, p.ws, 6, wait_ns)) break;
         ++qc;
-        // S for the item's first two tiles
-        for (int j = 0; ok && j < 2 && j < n_kv; ++j) {
-          const int gg = g + j;
-          ok = wait_bounded(k_full + (gg & 1), (gg >> 1) & 1, abort_flag, p.ws, 7);
+        for (int j = 0; j < n_kv; ++j, ++g) {
+          const int b = g & 1;
+          // S_g overwrites the P that PV_{g-2} read
+          ok = wait_bounded(k_full + b, (g >> 1) & 1, abort_flag, p.ws, 7, wait_ns) &&
+               (g < 2 || wait_bounded(s_free + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 11, wait_ns));
           if (!ok) break;
           tc_fence_after();
-          issue_s(gg);
-          umma_commit(k_empty + (gg & 1));
+          const uint32_t kbase = sK + b * C::KV_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t qoff = (kk >> 2) * C::QBOX + (kk & 3) * 32;
+            const uint32_t koff = (kk >> 2) * C::KVBOX + (kk & 3) * 32;
+            umma_bf16_ss(tmem + C::TM_S + 64u * b, smem_desc_sw128(sQ + qoff, 16, 1024),
+                         smem_desc_sw128(kbase + koff, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(k_empty + b);
           if (j == n_kv - 1) umma_commit(q_empty);
-          umma_commit(s_full + (gg & 1));
+          umma_commit(s_full + b);
         }
-        for (int j = 0; ok && j < n_kv; ++j, ++g) {
+      }
+      // every commit above has landed before the block can exit
+      umma_commit(drain);
+      drain_wait(drain, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      const uint32_t sV = smem_u32(smem + C::OFF_V);
+      int g = 0, oc = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int i = take_item(k, 19);
+        if (i < 0) break;
+        const int n_kv = p.tiles[item_of(i, p.n_tiles, G).tile_id].n_kv_tiles;
+        if (n_kv == 0) continue;
+        for (int j = 0; j < n_kv; ++j, ++g) {
           const int b = g & 1;
-          ok = wait_bounded(p_full + b, (g >> 1) & 1, abort_flag, p.ws, 8) &&
-               wait_bounded(v_full + b, (g >> 1) & 1, abort_flag, p.ws, 9);
+          ok = wait_bounded(p_full + b, (g >> 1) & 1, abort_flag, p.ws, 8, wait_ns) &&
+               wait_bounded(v_full + b, (g >> 1) & 1, abort_flag, p.ws, 9, wait_ns);
           // the first PV of an item overwrites O: the previous item's epilogue must have read it
-          if (ok && j == 0 && oc > 0) ok = wait_bounded(o_free, (oc - 1) & 1, abort_flag, p.ws, 10);
+          if (ok && j == 0 && oc > 0) ok = wait_bounded(o_free, (oc - 1) & 1, abort_flag, p.ws, 10, wait_ns);
           if (!ok) break;
           tc_fence_after();
           const uint32_t vbase = sV + b * C::KV_BYTES;
@@ -314,27 +333,17 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
             umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 64u * b + 8 * kk,
                          smem_desc_sw128(vbase + kk * 2048, C::KVBOX, 1024), IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(v_empty + b);
+          umma_commit(s_free + b);
           umma_commit(o_done);
           if (j == n_kv - 1) umma_commit(o_final);
-          if (j + 2 < n_kv) {
-            const int gg = g + 2;
-            ok = wait_bounded(k_full + b, (gg >> 1) & 1, abort_flag, p.ws, 11);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(gg);
-            umma_commit(k_empty + b);
-            if (j + 2 == n_kv - 1) umma_commit(q_empty);
-            umma_commit(s_full + b);
-          }
         }
         ++oc;
       }
-      // every commit above has landed before the block can exit
-      umma_commit(drain);
-      drain_wait(drain, 0);
+      umma_commit(drain2);
+      drain_wait(drain2, 0);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ softmax
+  } else {
+    // ------------------------------------------------------------ softmax and epilogue
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
@@ -345,18 +354,19 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
       const int i = take_item(k, 12);
       if (!__all_sync(0xffffffffu, i != -2)) break;
       if (i < 0) break;
-      const int tile_id = item_of(i, p.n_tiles, G).tile_id;
-      const int n_kv = p.tiles[tile_id].n_kv_tiles;
-      const int q_pos = p.tiles[tile_id].q_pos0 + row;
-      const int q_pos0 = p.tiles[tile_id].q_pos0;
+      const Item it = item_of(i, p.n_tiles, G);
+      const QTile tile = p.tiles[it.tile_id];
+      const int n_kv = tile.n_kv_tiles;
+      const int q_pos = tile.q_pos0 + row;
+      const int q_pos0 = tile.q_pos0;
       float m_ref = -INFINITY, l = 0.f;
-      PieceCursor cur{p.tiles[tile_id].run_begin, 0, p.tiles[tile_id].run_end};
+      PieceCursor cur{tile.run_begin, 0, tile.run_end};
       for (int j = 0; j < n_kv; ++j, ++g) {
         const Piece pc = cur.next(p.runs);
         const bool tile_mask = (pc.len < 64) || (pc.causal && pc.pos0 + 63 > q_pos0);
         const int b = g & 1;
 
-        if (!__all_sync(0xffffffffu, wait_bounded(s_full + b, (g >> 1) & 1, abort_flag, p.ws, 13))) {
+        if (!__all_sync(0xffffffffu, wait_bounded(s_full + b, (g >> 1) & 1, abort_flag, p.ws, 13, wait_ns))) {
           ok = false;
           break;
         }
@@ -410,7 +420,7 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
         tmem_st32(tl + C::TM_S + 64u * b, pk);  // P over the first 32 columns of this S buffer
         if (__any_sync(0xffffffffu, scale_o)) {
           // O may only be rescaled once PV_{g-1} (still in flight) has landed
-          if (!__all_sync(0xffffffffu, wait_bounded(o_done, (g - 1) & 1, abort_flag, p.ws, 14))) {
+          if (!__all_sync(0xffffffffu, wait_bounded(o_done, (g - 1) & 1, abort_flag, p.ws, 14, wait_ns))) {
             ok = false;
             break;
           }
@@ -430,35 +440,10 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
         mbar_arrive(p_full + b);
       }
       if (!ok) break;
+      // ---- epilogue of the item: O/l and the LSE at the output rows
       if (n_kv > 0) {
-        // the row's running max and sum for the epilogue warps
-        stats[(oc & 1) * 128 + row] = make_float2(m_ref, l);
-        mbar_arrive(stats_full);
-        ++oc;
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-    int oc = 0;
-    for (int k = 0;; ++k) {
-      const int i = take_item(k, 16);
-      if (!__all_sync(0xffffffffu, i != -2)) break;
-      if (i < 0) break;
-      const Item it = item_of(i, p.n_tiles, G);
-      const QTile tile = p.tiles[it.tile_id];
-      const int n_kv = tile.n_kv_tiles;
-      float m_raw = -INFINITY, l = 0.f;
-      if (n_kv > 0) {
-        if (!__all_sync(0xffffffffu, wait_bounded(o_final, oc & 1, abort_flag, p.ws, 15) &&
-                                         wait_bounded(stats_full, oc & 1, abort_flag, p.ws, 17)))
-          break;
+        if (!__all_sync(0xffffffffu, wait_bounded(o_final, oc & 1, abort_flag, p.ws, 15, wait_ns))) break;
         tc_fence_after();
-        const float2 st = stats[(oc & 1) * 128 + row];
-        m_raw = st.x;
-        l = st.y;
       }
       const bool valid_row = row < tile.q_rows;
       const bool has = l > 0.f;
@@ -497,7 +482,7 @@ __global__ void __launch_bounds__(320, 2) attn_fwd_tc_kernel(const __grid_consta
           }
         }
       }
-      if (valid_row) p.lse[(int64_t)it.h * p.lse_ld + out_row] = has ? m_raw * p.scale + logf(l) : -INFINITY;
+      if (valid_row) p.lse[(int64_t)it.h * p.lse_ld + out_row] = has ? m_ref * p.scale + logf(l) : -INFINITY;
       if (n_kv > 0) ++oc;
     }
   }
@@ -529,7 +514,7 @@ static cudaError_t launch_tc(const TcParams& p, int n_blocks, cudaStream_t strea
   const uint32_t smem = TcCfg<D>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<n_blocks, 320, smem, stream>>>(p);
+  kern<<<n_blocks, 224, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

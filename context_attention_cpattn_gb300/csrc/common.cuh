@@ -60,17 +60,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete.  Returns false
 // if the block is aborting or the wait ran out of time (then the fault is
-// recorded and the abort flag raised for the other warps).
+// recorded and the abort flag raised for the other warps).  The limit is 4 s
+// unless the kernel passes another (the forward takes a shorter one from the
+// workspace header when a fault-path test asks for it).
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                             WsHeader* ws, uint32_t where) {
+                                             WsHeader* ws, uint32_t where, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit_ns) {
       record_fault(ws, CPATTN_FAULT_WAIT_TIMEOUT, where);
       *abort_flag = 1;
       return false;

@@ -38,7 +38,9 @@ typedef struct WsHeader {
   uint32_t info;      // where (block index)
   uint32_t detail;    // which wait / value
   uint32_t next_item; // work counter of persistent kernels (items handed out beyond the first wave)
-  uint32_t pad[60];
+  uint32_t wait_limit_us;  // fault-path test support: limit of every bounded wait (0 = the default)
+  uint32_t withhold;       // fault-path test support: 1 = the forward's block 0 never loads its first V tile
+  uint32_t pad[58];
 } WsHeader;
 
 #ifdef __cplusplus

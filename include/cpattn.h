@@ -502,6 +502,23 @@ cpattn_status_t cpattn_dcp_sweep(const int64_t* seqlens, int64_t n, const cpattn
  * The fault word is cleared by the next cpattn_fwd / cpattn_block_fwd. */
 cpattn_status_t cpattn_sync_status(const void* workspace, void* stream);
 
+/* Test support for the device fault path (not for production use).
+ * Process-wide settings applied to the workspace of every later cpattn_fwd,
+ * cpattn_block_fwd, cpattn_bwd and cpattn_block_bwd call:
+ *   wait_limit_us: every bounded wait inside the kernels gives up after this
+ *     many microseconds instead of the default 4 s (0 restores the default);
+ *   withhold_first_v: nonzero makes block 0 of the bf16 forward skip loading
+ *     its first V tile, so the MMA thread's wait for it (and the waits of the
+ *     warps behind it) run out: the kernel records a wait timeout (fault code
+ *     1, block 0, the site that ran out first) in the workspace, lets
+ *     its copies in flight land, frees its tensor memory and returns early;
+ *     the output is then incomplete and cpattn_sync_status reports
+ *     CPATTN_DEVICE_FAULT.
+ * No GPU fault, trap or hang is involved: only a wait that nothing completes,
+ * ended by its time limit.  Errors: CPATTN_INVALID_ARG for withhold_first_v
+ * without a limit, or a limit above 10 s. */
+cpattn_status_t cpattn_debug_wait_fault(uint32_t wait_limit_us, int32_t withhold_first_v);
+
 /* Message of the last failed call on this thread ("" if none). */
 const char* cpattn_last_error_string(void);
 

@@ -197,3 +197,14 @@ def test_merge_permute_and_loss_argument_errors(cpattn):
     assert L.cpattn_scatter_rows(fake, fake, 10, fake, -3, 32, None) == cpattn.INVALID_ARG
     assert L.cpattn_token_loss_norm(None, fake, 10, fake, fake, None, None) == cpattn.INVALID_ARG
     assert L.cpattn_token_loss_norm(fake, fake, -1, fake, fake, None, None) == cpattn.INVALID_ARG
+
+
+def test_fault_path_test_settings_reject_bad_arguments(cpattn):
+    """The fault-path test settings (host only, nothing launched)."""
+    with pytest.raises(cpattn.CpattnError) as e:
+        cpattn.cpattn_debug_wait_fault(0, True)          # a withheld load needs a short limit
+    assert e.value.status == cpattn.INVALID_ARG
+    with pytest.raises(cpattn.CpattnError):
+        cpattn.cpattn_debug_wait_fault(20_000_000, False)  # above 10 s
+    cpattn.cpattn_debug_wait_fault(1000, True)
+    cpattn.cpattn_debug_wait_fault(0, False)             # back to the defaults

@@ -18,9 +18,10 @@ import pytest
 
 from oracle import teacher_forcing as TF
 
-# Kernel tile shapes: (rows per tile, keys or queries per piece).
-FWD_TILES = {"bf16": (128, 64), "fp32": (64, 32)}
-BWD_TILES = {"bf16": (128, 64), "fp32": (32, 64)}
+# Kernel tile shapes: (rows per tile, keys or queries per piece, pieces per
+# kernel tile).
+FWD_TILES = {"bf16": (128, 64, 1), "fp32": (64, 32, 1)}
+BWD_TILES = {"bf16": (128, 64, 1), "fp32": (32, 64, 1)}
 
 
 def seq_pos(cu):
@@ -55,7 +56,7 @@ def rank_maps(plan, gathered):
 
 
 def replay(tiles, runs, tok_of_row, seq, pos, causal, tile_rows, piece, backward, rank_of_tok=None, cp=None,
-           q_rank=None, step=None, local=None, gathered=False):
+           q_rank=None, step=None, local=None, gathered=False, per_tile=1):
     """Pair counts [query token, key token] of a work list, with the structural
     checks of every tile and run.  The positions a list carries are the
     tokens' positions in their sequence, except on gathered grid2d rows
@@ -98,7 +99,7 @@ def replay(tiles, runs, tok_of_row, seq, pos, causal, tile_rows, piece, backward
                 if q_rank is not None:
                     assert t == step
         assert steps == sorted(steps), "runs out of ring order"
-        assert pieces == n_pieces
+        assert pieces == -(-n_pieces // per_tile)
     return count, seen
 
 
@@ -124,10 +125,10 @@ def test_whole_call_visits_every_allowed_pair_once(cpattn, case, backward, dtype
     plan = cpattn.cpattn_plan(cu, cp, mode, grid)
     tok_of_row, rank_of_tok, _ = rank_maps(plan, mode == "grid2d")
     seq, pos = seq_pos(cu)
-    rows, piece = (BWD_TILES if backward else FWD_TILES)[dtype]
+    rows, piece, per = (BWD_TILES if backward else FWD_TILES)[dtype]
     tiles, runs = plan.worklist(backward, dtype, causal)
     count, seen = replay(tiles, runs, tok_of_row, seq, pos, causal, rows, piece, backward, rank_of_tok, cp,
-                         gathered=(mode == "grid2d"))
+                         gathered=(mode == "grid2d"), per_tile=per)
     assert (seen == 1).all()
     assert np.array_equal(count, definition(cu, causal).astype(np.int32))
 
@@ -139,13 +140,13 @@ def test_ring_steps_partition_the_pairs(cpattn, case, backward):
     plan = cpattn.cpattn_plan(cu, cp, mode, grid)
     tok_of_row, rank_of_tok, local = rank_maps(plan, mode == "grid2d")
     seq, pos = seq_pos(cu)
-    rows, piece = (BWD_TILES if backward else FWD_TILES)["bf16"]
+    rows, piece, per = (BWD_TILES if backward else FWD_TILES)["bf16"]
     total = np.zeros((len(seq), len(seq)), dtype=np.int32)
     for r in range(cp):
         for t in range(cp):
             tiles, runs = plan.worklist(backward, "bf16", causal, r, t)
             count, seen = replay(tiles, runs, tok_of_row, seq, pos, causal, rows, piece, backward, rank_of_tok, cp,
-                                 q_rank=r, step=t, local=local, gathered=(mode == "grid2d"))
+                                 q_rank=r, step=t, local=local, gathered=(mode == "grid2d"), per_tile=per)
             # forward: every query row of rank r once per step; backward: every key row of rank (r - t) mod cp
             owner = r if not backward else (r - t) % cp
             assert (seen[rank_of_tok == owner] == 1).all() and (seen[rank_of_tok != owner] == 0).all()
@@ -180,7 +181,7 @@ def test_head_sharded_lists_cover_every_group(cpattn, kind):
                 assert masked == 0
     # paired lists carry no position mask (every run is fully visible under the
     # teacher-forcing mask), so they are replayed as unmasked lists
-    count, seen = replay(tiles, runs, tok_of_row, seq, pos, kind == "mesh", 128, 64, False)
+    count, seen = replay(tiles, runs, tok_of_row, seq, pos, kind == "mesh", 128, 64, False, per_tile=1)
     assert (seen == u).all()
     assert np.array_equal(count, u * want.astype(np.int32))
 
@@ -217,10 +218,10 @@ def test_random_layouts(cpattn, seed):
             for causal in (True, False):
                 for backward in (False, True):
                     dtype = ("bf16", "fp32")[int(rng.integers(0, 2))]
-                    rows, piece = (BWD_TILES if backward else FWD_TILES)[dtype]
+                    rows, piece, per = (BWD_TILES if backward else FWD_TILES)[dtype]
                     tiles, runs = plan.worklist(backward, dtype, causal)
                     count, seen = replay(tiles, runs, tok_of_row, seq, pos, causal, rows, piece, backward,
-                                         rank_of_tok, cp)
+                                         rank_of_tok, cp, per_tile=per)
                     assert (seen == 1).all()
                     assert np.array_equal(count, definition(cu, causal).astype(np.int32)), (cu, cp, mode, causal)
     for cp in (2, 4, 6, 8):
@@ -233,10 +234,10 @@ def test_random_layouts(cpattn, seed):
         seq, pos = seq_pos(cu)
         tok_of_row, rank_of_tok, _ = rank_maps(plan, True)
         for backward in (False, True):
-            rows, piece = (BWD_TILES if backward else FWD_TILES)["bf16"]
+            rows, piece, per = (BWD_TILES if backward else FWD_TILES)["bf16"]
             tiles, runs = plan.worklist(backward, "bf16", False)
             count, seen = replay(tiles, runs, tok_of_row, seq, pos, False, rows, piece, backward, rank_of_tok, cp,
-                                 gathered=True)
+                                 gathered=True, per_tile=per)
             assert (seen == 1).all() and np.array_equal(count, definition(cu, False).astype(np.int32))
     for u, r in ((2, 2), (4, 1), (1, 4), (2, 3)):
         lens = rng.integers(2 * r, 240, size=rng.integers(1, 5))
@@ -246,5 +247,5 @@ def test_random_layouts(cpattn, seed):
         seq, pos = seq_pos(cu)
         tok_of_row = plan.index_map()[np.arange(u * T) % T]
         tiles, runs = plan.worklist(False, "bf16", True)
-        count, seen = replay(tiles, runs, tok_of_row, seq, pos, True, 128, 64, False)
+        count, seen = replay(tiles, runs, tok_of_row, seq, pos, True, 128, 64, False, per_tile=1)
         assert (seen == u).all() and np.array_equal(count, u * definition(cu, True).astype(np.int32)), (cu, u, r)
