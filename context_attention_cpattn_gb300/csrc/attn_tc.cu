@@ -143,18 +143,15 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
   uint64_t* k_full = bars + 2;     // [2]
-  uint64_t* k_empty = bars + 4;    // [2]
+  uint64_t* s_done = bars + 4;     // [2] S_j has run: K_j's buffer is free, the softmax may read S_j
   uint64_t* v_full = bars + 6;     // [2]
-  uint64_t* v_empty = bars + 8;    // [2]
-  uint64_t* s_full = bars + 10;    // [2]
+  uint64_t* pv_done = bars + 8;    // [2] PV_j has run: V_j's buffer and P_j's S buffer are free, O holds it
   uint64_t* p_full = bars + 12;    // [2]
-  uint64_t* o_done = bars + 14;    // after every PV
   uint64_t* o_final = bars + 15;   // after an item's last PV
   uint64_t* o_free = bars + 16;    // the epilogue has read O
   uint64_t* drain = bars + 17;     // the S issuer's MMAs have landed
   uint64_t* item_full = bars + 18;   // [4] ring of work items handed from the producer
   uint64_t* item_empty = bars + 22;  // [4]
-  uint64_t* s_free = bars + 26;      // [2] PV_j has read P_j: the buffer may take S_{j+2}
   uint64_t* drain2 = bars + 28;      // the PV issuer's MMAs have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -173,14 +170,11 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
     mbar_init(q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(k_full + b, 1);
-      mbar_init(k_empty + b, 1);
+      mbar_init(s_done + b, 1);
       mbar_init(v_full + b, 1);
-      mbar_init(v_empty + b, 1);
-      mbar_init(s_full + b, 1);
+      mbar_init(pv_done + b, 1);
       mbar_init(p_full + b, 128);
-      mbar_init(s_free + b, 1);
     }
-    mbar_init(o_done, 1);
     mbar_init(o_final, 1);
     mbar_init(o_free, 128);
     mbar_init(drain, 1);
@@ -246,7 +240,7 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
         PieceCursor c{tile.run_begin, 0, tile.run_end};
         auto load_k = [&](int gk, int row) -> bool {
           const int b = gk & 1;
-          if (gk >= 2 && !wait_bounded(k_empty + b, ((gk >> 1) - 1) & 1, abort_flag, p.ws, 3, wait_ns)) return false;
+          if (gk >= 2 && !wait_bounded(s_done + b, ((gk >> 1) - 1) & 1, abort_flag, p.ws, 3, wait_ns)) return false;
           mbar_arrive_expect_tx(k_full + b, C::KV_BYTES);
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_3d(smem + C::OFF_K + b * C::KV_BYTES + kb * C::KVBOX, &p.tm_k, k_full + b, kb * 64, it.g, row);
@@ -262,7 +256,7 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
             row_next = c.next(p.runs).row0;
             if (!load_k(g + 1, row_next)) { ok = false; break; }
           }
-          if (g >= 2 && !wait_bounded(v_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 4, wait_ns)) { ok = false; break; }
+          if (g >= 2 && !wait_bounded(pv_done + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 4, wait_ns)) { ok = false; break; }
           if (withhold_v0 && g == 0) continue;
           mbar_arrive_expect_tx(v_full + b, C::KV_BYTES);
           for (int kb = 0; kb < C::KB; ++kb)
@@ -288,7 +282,7 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
           const int b = g & 1;
           // S_g overwrites the P that PV_{g-2} read
           ok = wait_bounded(k_full + b, (g >> 1) & 1, abort_flag, p.ws, 7, wait_ns) &&
-               (g < 2 || wait_bounded(s_free + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 11, wait_ns));
+               (g < 2 || wait_bounded(pv_done + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 11, wait_ns));
           if (!ok) break;
           tc_fence_after();
           const uint32_t kbase = sK + b * C::KV_BYTES;
@@ -299,9 +293,8 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
             umma_bf16_ss(tmem + C::TM_S + 64u * b, smem_desc_sw128(sQ + qoff, 16, 1024),
                          smem_desc_sw128(kbase + koff, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
           }
-          umma_commit(k_empty + b);
           if (j == n_kv - 1) umma_commit(q_empty);
-          umma_commit(s_full + b);
+          umma_commit(s_done + b);
         }
       }
       // every commit above has landed before the block can exit
@@ -332,9 +325,7 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
           for (int kk = 0; kk < 4; ++kk)  // 16 keys per MMA: P columns 8kk.., V rows 16kk..
             umma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 64u * b + 8 * kk,
                          smem_desc_sw128(vbase + kk * 2048, C::KVBOX, 1024), IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(v_empty + b);
-          umma_commit(s_free + b);
-          umma_commit(o_done);
+          umma_commit(pv_done + b);
           if (j == n_kv - 1) umma_commit(o_final);
         }
         ++oc;
@@ -366,7 +357,7 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
         const bool tile_mask = (pc.len < 64) || (pc.causal && pc.pos0 + 63 > q_pos0);
         const int b = g & 1;
 
-        if (!__all_sync(0xffffffffu, wait_bounded(s_full + b, (g >> 1) & 1, abort_flag, p.ws, 13, wait_ns))) {
+        if (!__all_sync(0xffffffffu, wait_bounded(s_done + b, (g >> 1) & 1, abort_flag, p.ws, 13, wait_ns))) {
           ok = false;
           break;
         }
@@ -420,7 +411,8 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
         tmem_st32(tl + C::TM_S + 64u * b, pk);  // P over the first 32 columns of this S buffer
         if (__any_sync(0xffffffffu, scale_o)) {
           // O may only be rescaled once PV_{g-1} (still in flight) has landed
-          if (!__all_sync(0xffffffffu, wait_bounded(o_done, (g - 1) & 1, abort_flag, p.ws, 14, wait_ns))) {
+          if (!__all_sync(0xffffffffu,
+                          wait_bounded(pv_done + ((g - 1) & 1), ((g - 1) >> 1) & 1, abort_flag, p.ws, 14, wait_ns))) {
             ok = false;
             break;
           }
