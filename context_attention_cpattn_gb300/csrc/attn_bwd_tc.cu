@@ -158,7 +158,6 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
   uint64_t* p_full = bars + 10;    // [2]
   uint64_t* dp_full = bars + 12;
   uint64_t* ds_full = bars + 13;
-  uint64_t* dq_full = bars + 14;
   uint64_t* dq_free = bars + 15;
   uint64_t* acc_done = bars + 16;  // the item's last dK / dV MMA has run
   uint64_t* acc_free = bars + 17;  // the epilogue has read dK / dV
@@ -193,7 +192,6 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
     }
     mbar_init(dp_full, 1);
     mbar_init(ds_full, 128);
-    mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
     mbar_init(acc_done, 1);
     mbar_init(acc_free, 128);
@@ -518,7 +516,8 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
       for (int t = 0; t < n; ++t, ++g) {
         const Piece pc = cur.next(p.runs);
         const int sb = g & 1;
-        if (!__all_sync(0xffffffffu, wait_bounded(dq_full, g & 1, abort_flag, p.ws, 20))) {
+        // every MMA of piece g, dQ^T_g the last, has run
+        if (!__all_sync(0xffffffffu, wait_bounded(qd_empty + (g & 1), (g >> 1) & 1, abort_flag, p.ws, 20))) {
           ok = false;
           break;
         }
@@ -600,8 +599,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
           for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T: 16 keys per MMA
             umma_bf16_ss(tmem + C::TM_DQ, smem_desc_sw128(sK + kk * 2048, C::KBOX, 1024),
                          smem_desc_sw128(dsb + kk * 2048, C::DS_BYTES, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
-          umma_commit(qd_empty + b);
-          umma_commit(dq_full);
+          umma_commit(qd_empty + b);  // also tells the dQ warps that dQ^T_g is ready
           if (t == n - 1) {
             umma_commit(acc_done);
             umma_commit(kv_empty);
