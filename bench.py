@@ -815,6 +815,43 @@ def run_aux(args):
         valid = (torch.rand(Tl, device=dev, generator=g) > 0.1).to(torch.uint8)
         sec = timeit(lambda: cp.cpattn_token_loss_norm(loss, valid, res, cnt))
         record("loss_norm_kernel", f"T={Tl}", Tl * 5, sec)
+    # host link: pinned host memory to and from HBM, 805 MB (the micro-batch's Q, K and V),
+    # by copy engines (cudaMemcpyAsync on 1 or 3 streams) and by the copy kernel reading or
+    # writing host memory directly
+    nb = 805306368
+    hbuf = torch.empty(nb, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(nb, dtype=torch.uint8, device=dev)
+    link = []
+
+    def rec(what, sec):
+        link.append({"what": what, "bytes": nb, "ms": sec * 1e3, "GB_s": nb / sec / 1e9})
+
+    rec("H2D cudaMemcpyAsync, 1 stream", timeit(lambda: dbuf.copy_(hbuf, non_blocking=True), reps=5))
+    streams = [torch.cuda.Stream(dev) for _ in range(3)]
+    thirds = [(i * nb // 3) // 16 * 16 for i in range(4)]
+
+    def three(h2d):
+        cur = torch.cuda.current_stream(dev)
+        evs = []
+        for si, st in enumerate(streams):
+            st.wait_stream(cur)
+            with torch.cuda.stream(st):
+                a, b = thirds[si], thirds[si + 1]
+                if h2d:
+                    dbuf[a:b].copy_(hbuf[a:b], non_blocking=True)
+                else:
+                    hbuf[a:b].copy_(dbuf[a:b], non_blocking=True)
+            evs.append(st)
+        for st in evs:
+            cur.wait_stream(st)
+
+    rec("H2D cudaMemcpyAsync, 3 streams", timeit(lambda: three(True), reps=5))
+    rec("D2H cudaMemcpyAsync, 1 stream", timeit(lambda: hbuf.copy_(dbuf, non_blocking=True), reps=5))
+    rec("D2H cudaMemcpyAsync, 3 streams", timeit(lambda: three(False), reps=5))
+    for blocks in (38, 152, 608):
+        rec(f"H2D copy kernel, {blocks} blocks", timeit(lambda: cp.cpattn_copy(dbuf, hbuf, n_blocks=blocks), reps=5))
+        rec(f"D2H copy kernel, {blocks} blocks", timeit(lambda: cp.cpattn_copy(hbuf, dbuf, n_blocks=blocks), reps=5))
+    del hbuf, dbuf
     # Dynamic-CP solver (host C++): the micro-batch count sweep over a global
     # batch of 2048 long-tailed samples, dp 8, pp 4, V 2, m = 4..16
     rng = np.random.default_rng(3)
@@ -824,7 +861,8 @@ def run_aux(args):
         r = cp.cpattn_dcp_sweep(L, 8, 4, 2, 4, 8, 16384, 4 * 128 * 32, 0)
     host = [{"solver": "cpattn_dcp_sweep", "shape": "2048 samples, dp 8, pp 4, V 2, m 4..16 (13 schedules)",
              "ms": (time.perf_counter() - t0) / reps * 1e3, "knee_m": r["knee_m"], "best_m": r["best_m"]}]
-    print(json.dumps({"aux": out, "host": host, "hbm_peak_GB_s": peak, "peak_source": src}), flush=True)
+    print(json.dumps({"aux": out, "host_link": link, "host": host, "hbm_peak_GB_s": peak, "peak_source": src}),
+          flush=True)
 
 
 def main(argv=None):

@@ -88,6 +88,7 @@ _SIGNATURES = {
     "cpattn_sync_status": [_P, _P],
     "cpattn_static_sync_status": [_P],
     "cpattn_debug_wait_fault": [ctypes.c_uint32, _I32],
+    "cpattn_copy": [_P, _P, _SZ, _I32, _P],
     "cpattn_last_error_string": [],
     "cpattn_version": [],
 }
@@ -374,6 +375,15 @@ def cpattn_fwd_flops(cu_seqlens, H: int, D: int, causal: bool) -> int:
 
 def cpattn_sync_status(workspace=None, stream=None):
     _check(lib().cpattn_sync_status(_ptr(workspace), _stream(stream)))
+
+
+def cpattn_copy(dst, src, n_blocks: int = 0, stream=None):
+    """dst <- src with a copy kernel; either tensor may be pinned host memory
+    (read or written by the GPU over the host link)."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src sizes differ")
+    _check(lib().cpattn_copy(_ptr(dst), _ptr(src), nbytes, int(n_blocks), _stream(stream)))
 
 
 def cpattn_debug_wait_fault(wait_limit_us: int, withhold_first_v: bool = False):

@@ -858,6 +858,32 @@ cpattn_status_t cpattn_fwd_flops(const int32_t* cu, int32_t n_seqs, int32_t H, i
   return CPATTN_OK;
 }
 
+// Device-side address of a pointer the GPU can reach: device memory as is,
+// pinned (registered) host memory through its mapped address; else NULL.
+static const void* device_reachable(const void* ptr) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return ptr;
+  if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+  return nullptr;
+}
+
+cpattn_status_t cpattn_copy(void* dst, const void* src, size_t bytes, int32_t n_blocks, void* stream) {
+  if (bytes == 0) return CPATTN_OK;
+  if (!dst || !src) return fail(CPATTN_INVALID_ARG, "dst and src must not be NULL");
+  if ((bytes & 15) || !aligned16(dst) || !aligned16(src))
+    return fail(CPATTN_INVALID_ARG, "dst and src must be 16-byte aligned and bytes a multiple of 16");
+  const void* s = device_reachable(src);
+  void* d = const_cast<void*>(device_reachable(dst));
+  if (!s || !d) return fail(CPATTN_INVALID_ARG, "dst and src must be device memory or pinned host memory");
+  cudaError_t e = cpattn::launch_copy(s, d, (int64_t)bytes, n_blocks, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy kernel launch");
+  return CPATTN_OK;
+}
+
 cpattn_status_t cpattn_debug_wait_fault(uint32_t wait_limit_us, int32_t withhold_first_v) {
   if (withhold_first_v != 0 && wait_limit_us == 0)
     return fail(CPATTN_INVALID_ARG, "withholding a load needs a short wait limit (wait_limit_us > 0)");

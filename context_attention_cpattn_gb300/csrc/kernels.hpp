@@ -113,6 +113,11 @@ cudaError_t launch_permute_rows(const void* src, void* dst, const int64_t* index
 cudaError_t launch_lse_regroup(const float* src, float* dst, const int64_t* a2a, int Hs, int u, int64_t T,
                                cudaStream_t stream);
 
+// dst[0, bytes) = src[0, bytes): 16-byte aligned, bytes a multiple of 16;
+// either pointer may be pinned host memory the device can address.
+// n_blocks <= 0: four blocks per SM.
+cudaError_t launch_copy(const void* src, void* dst, int64_t bytes, int n_blocks, cudaStream_t stream);
+
 int num_sms();
 
 // TMA tensor maps of a [rows, heads, D] tensor viewed as (D, heads, rows):

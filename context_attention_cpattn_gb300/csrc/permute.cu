@@ -40,7 +40,34 @@ __global__ void __launch_bounds__(256) lse_regroup_kernel(const float* __restric
   }
 }
 
+// Plain copy of n 16-byte vectors, four loads in flight per thread.  Either
+// side may be pinned host memory that the GPU reads or writes over the
+// host link (NVLink-C2C on Grace hosts).
+__global__ void __launch_bounds__(256) copy_vec_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                       int64_t n) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n; i += 4 * stride) {
+    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+    dst[i] = a;
+    dst[i + stride] = b;
+    dst[i + 2 * stride] = c;
+    dst[i + 3 * stride] = d;
+  }
+  for (; i < n; i += stride) dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_copy(const void* src, void* dst, int64_t bytes, int n_blocks, cudaStream_t stream) {
+  if (bytes == 0) return cudaSuccess;
+  const int64_t n = bytes / 16;
+  const int64_t want = (n + 255) / 256;
+  const int64_t cap = n_blocks > 0 ? n_blocks : (int64_t)num_sms() * 4;
+  copy_vec_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, stream>>>(static_cast<const uint4*>(src),
+                                                                           static_cast<uint4*>(dst), n);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_lse_regroup(const float* src, float* dst, const int64_t* a2a, int Hs, int u, int64_t T,
                                cudaStream_t stream) {

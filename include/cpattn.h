@@ -369,6 +369,18 @@ cpattn_status_t cpattn_gather_rows(const void* src, int64_t src_rows, void* dst,
 cpattn_status_t cpattn_scatter_rows(const void* src, void* dst, int64_t dst_rows, const int64_t* index,
                                     int64_t rows, int64_t row_bytes, void* stream);
 
+/* Copy `bytes` from src to dst with a kernel, so that either side can be
+ * pinned host memory that the GPU reads or writes directly over the host link
+ * (NVLink-C2C on Grace hosts) instead of through a copy engine.  The pages
+ * have no counterpart: this serves the end-to-end path that brings each
+ * step's inputs from the host.
+ *   dst, src: device memory or pinned (registered) host memory, 16-byte
+ *     aligned, not overlapping; bytes a multiple of 16.
+ *   n_blocks: thread blocks of 256 threads (<= 0: four per SM); fewer blocks
+ *     leave room on the SMs for kernels running beside the copy.
+ *   Errors: CPATTN_INVALID_ARG for NULL, misaligned or pageable pointers. */
+cpattn_status_t cpattn_copy(void* dst, const void* src, size_t bytes, int32_t n_blocks, void* stream);
+
 /* Bytes of device scratch compiled into the library for cpattn_fwd_static. */
 #define CPATTN_STATIC_SCRATCH_BYTES (8u << 20)
 

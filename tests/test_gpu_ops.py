@@ -175,3 +175,28 @@ def test_device_fault_word_reports_nothing_on_clean_runs(cp):
     cp.cpattn_fwd(plan, qd, kd, vd, o, lse, ws)
     cp.cpattn_sync_status(ws)
     assert int(ws[:4].view(torch.int32).item()) == 0
+
+
+def test_copy_kernel_between_pinned_host_and_device(cp):
+    """cpattn_copy moves bytes exactly: pinned host -> device, device -> pinned
+    host, device -> device, with a few and with many blocks."""
+    g = torch.Generator().manual_seed(3)
+    h = torch.randint(0, 2 ** 31 - 1, (3 << 20,), generator=g, dtype=torch.int32).pin_memory()
+    d = torch.empty(h.shape, dtype=torch.int32, device="cuda")
+    for blocks in (3, 0):
+        d.fill_(-1)
+        cp.cpattn_copy(d, h, n_blocks=blocks)
+        torch.cuda.synchronize()
+        assert torch.equal(d.cpu(), h)
+        back = torch.full(h.shape, -1, dtype=torch.int32).pin_memory()
+        cp.cpattn_copy(back, d, n_blocks=blocks)
+        torch.cuda.synchronize()
+        assert torch.equal(back, h)
+    d2 = torch.empty_like(d)
+    cp.cpattn_copy(d2, d)
+    torch.cuda.synchronize()
+    assert torch.equal(d2, d)
+    with pytest.raises(cp.CpattnError):
+        cp.cpattn_copy(d[1:3], d[5:7])          # 8 bytes: not a multiple of 16
+    with pytest.raises(cp.CpattnError):
+        cp.cpattn_copy(d, torch.empty(h.shape, dtype=torch.int32))   # pageable host memory
