@@ -26,6 +26,9 @@ add up to the full gradients.
 
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 from .attention import causal_visible, kv_head, packed_attention, seq_ids_and_positions, to_f64
@@ -101,35 +104,69 @@ def block_attention_bwd(q, k, v, dout, O, LSE, cu_seqlens, q_rows, kv_rows, caus
     return dQ, dK, dV
 
 
-def dq_at_rows(q, k, v, dout, cu_seqlens, rows, causal: bool, scale: float):
+def dq_at_rows(q, k, v, dout, cu_seqlens, rows, causal: bool, scale: float,
+               threads: int | None = None, batch: int | None = None):
     """dQ [R,H,D] of the sampled query rows ``rows`` (all heads), each from
-    its full definition: the row's own forward (lse, O, delta) over its
-    sequence's allowed keys, then dS and dQ.  For sizes where the whole
-    backward is too large for the CPU."""
+    its full definition: the row's own forward (P, O, delta) over its
+    sequence's allowed keys, then dP, dS and dQ as in the module docstring.
+    For sizes where the whole backward is too large for the CPU.
+
+    For each KV head and each sequence holding a sampled row, the keys and
+    values up to the last sampled row are converted to fp64 once.  The rows
+    are cut into batches (the query heads that read the KV head stacked in
+    one matrix product; at most ``batch`` rows, fewer where the score matrix
+    would pass 2**24 entries or where fewer batches than threads would be
+    left) that run on one thread pool, largest first (numpy releases the
+    GIL).  The causal rule sets the scores of the keys after each query's
+    position to -inf; P and dS are formed in place in the score and dP
+    temporaries."""
     rows = np.asarray(rows, dtype=np.int64)
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     H, D = q.shape[1], q.shape[2]
     Hkv = k.shape[1]
+    G = H // Hkv
     seq = np.searchsorted(cu, rows, side="right") - 1
+    qr, dor = to_f64(q[rows]), to_f64(dout[rows])
     dQ = np.zeros((len(rows), H, D))
-    for s in np.unique(seq):
-        idx = np.nonzero(seq == s)[0]
-        a, b = int(cu[s]), int(cu[s + 1])
-        kend = int(rows[idx].max()) + 1 if causal else b
+    threads = threads or max(1, len(os.sched_getaffinity(0)))
+    batch = batch or max(16, 128 // G)    # about 128 (row, head) pairs per matrix product
+
+    def work(idx, heads, a, n, Kg, Vg):
+        rr = rows[idx]
+        Qb = qr[idx][:, heads, :].reshape(len(idx) * G, D)
+        dOb = dor[idx][:, heads, :].reshape(len(idx) * G, D)
+        S = Qb @ Kg[:n].T
+        S *= scale
+        if causal:
+            for r, qpos in enumerate(np.repeat(rr - a, G)):
+                S[r, qpos + 1:] = -np.inf     # keys after the query's position
+        S -= S.max(axis=1, keepdims=True)
+        P = np.exp(S, out=S)
+        P /= P.sum(axis=1, keepdims=True)
+        O = P @ Vg[:n]
+        delta = np.sum(dOb * O, axis=1)
+        dS = dOb @ Vg[:n].T                   # dP
+        dS -= delta[:, None]
+        dS *= P
+        return idx, heads, (scale * (dS @ Kg[:n])).reshape(len(idx), G, D)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
         for g in range(Hkv):
-            Kg, Vg = to_f64(k[a:kend, g]), to_f64(v[a:kend, g])
-            for h in [h for h in range(H) if kv_head(h, H, Hkv) == g]:
-                Qr, dOr = to_f64(q[rows[idx], h]), to_f64(dout[rows[idx], h])
-                S = scale * (Qr @ Kg.T)
-                if causal:
-                    allowed = causal_visible(np.arange(kend - a)[None, :], (rows[idx] - a)[:, None])
-                    S = np.where(allowed, S, -np.inf)
-                m = S.max(axis=1, keepdims=True)
-                P = np.exp(S - m)
-                P /= P.sum(axis=1, keepdims=True)
-                O = P @ Vg
-                delta = np.sum(dOr * O, axis=1)
-                dP = dOr @ Vg.T
-                dS = P * (dP - delta[:, None])
-                dQ[idx, h] = scale * (dS @ Kg)
+            heads = [h for h in range(H) if kv_head(h, H, Hkv) == g]
+            assert len(heads) == G
+            tasks = []
+            for s in np.unique(seq):
+                idx_s = np.nonzero(seq == s)[0]
+                a, b = int(cu[s]), int(cu[s + 1])
+                kend_s = int(rows[idx_s].max()) + 1 if causal else b
+                Kg, Vg = to_f64(k[a:kend_s, g]), to_f64(v[a:kend_s, g])
+                bs = max(1, min(batch, (1 << 24) // (G * (kend_s - a)), -(-len(idx_s) // threads)))
+                for i in range(0, len(idx_s), bs):
+                    idx = idx_s[i:i + bs]
+                    n = (int(rows[idx].max()) + 1 if causal else b) - a
+                    tasks.append((len(idx) * n, idx, a, n, Kg, Vg))
+            tasks.sort(key=lambda t: -t[0])
+            for f in [ex.submit(work, idx, heads, a, n, Kg, Vg) for _, idx, a, n, Kg, Vg in tasks]:
+                idx, hs, dQb = f.result()
+                dQ[np.ix_(idx, hs)] = dQb
     return dQ

@@ -130,9 +130,13 @@ def test_ring_steps_sum_to_the_full_gradients(mode, cp, causal, grid):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-def test_dq_at_rows_equals_the_full_backward(causal):
+@pytest.mark.parametrize("threads,batch", [(None, None), (3, 2), (1, 1)])
+def test_dq_at_rows_equals_the_full_backward(causal, threads, batch):
+    """Row batches of any size, on any number of threads, give the full
+    backward's dQ rows (unsorted rows, several sequences, G = 2)."""
     cu, H, Hkv, D = (0, 40, 41, 90), 4, 2, 8
     q, k, v, do = _inputs(cu, H, Hkv, D, seed=8)
     full = B.packed_attention_bwd(q, k, v, do, cu, causal, 0.35)[0]
-    rows = np.array([0, 5, 39, 40, 41, 77, 89])
-    np.testing.assert_allclose(B.dq_at_rows(q, k, v, do, cu, rows, causal, 0.35), full[rows], rtol=1e-11, atol=1e-13)
+    rows = np.array([77, 0, 5, 39, 40, 41, 89, 12, 60])
+    got = B.dq_at_rows(q, k, v, do, cu, rows, causal, 0.35, threads=threads, batch=batch)
+    np.testing.assert_allclose(got, full[rows], rtol=1e-11, atol=1e-13)
