@@ -67,17 +67,37 @@ def test_static_scratch_forward_matches_workspace_forward(cp):
         U.check(second[0], second[1], O, L, w.dtype, f"{w.name} static vs oracle")
 
 
+def _buffers(T, H, Hkv, D):
+    """Device buffers that fit a call on T tokens, so that a call which
+    wrongly went ahead would still stay inside its buffers."""
+    q = torch.zeros(T, H, D, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(T, Hkv, D, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    o = torch.empty_like(q)
+    lse = torch.empty(H, T, dtype=torch.float32, device="cuda")
+    return [ctypes.c_void_p(t.data_ptr()) for t in (q, k, v)], ctypes.c_void_p(o.data_ptr()), \
+        ctypes.c_void_p(lse.data_ptr()), (q, k, v, o, lse)
+
+
 def test_static_scratch_rejects_what_it_cannot_hold(cp):
     L = cp.lib()
-    fake = ctypes.c_void_p(1 << 20)
     plans = [cp.cpattn_plan([0, 2 * 9 * 20], 4, "grid2d", (2, 9, 20)),
              cp.cpattn_plan_2d([0, 256], 2, 2),
              cp.cpattn_plan_paired([0, 64], 2, 4)]
+    (q, k, v), o, lse, keep = _buffers(2 * 9 * 20, 4, 4, 128)
     for plan in plans:
-        s = L.cpattn_fwd_static(plan.handle, fake, fake, fake, cp.DTYPE_BF16, 4, 4, 128, 0.1, 1, fake, fake, None)
+        s = L.cpattn_fwd_static(plan.handle, q, k, v, cp.DTYPE_BF16, 4, 4, 128, 0.1, 1, o, lse, None)
         assert s == cp.UNSUPPORTED, plan.mode
-    # many short sequences with a large cp: the work list outgrows the 8 MiB array
-    big = cp.cpattn_plan(np.arange(0, 64 * 2001, 64), 32, "zigzag")
-    s = L.cpattn_fwd_static(big.handle, fake, fake, fake, cp.DTYPE_BF16, 2, 2, 128, 0.1, 1, fake, fake, None)
+    # many short sequences with a large cp: every tile reads 2cp one-token
+    # chunks, and the work list outgrows the 8 MiB array (checked here on the
+    # host before the call)
+    n, ln = 10000, 64
+    big = cp.cpattn_plan(np.arange(0, ln * (n + 1), ln), 32, "zigzag")
+    tiles, runs = big.worklist(False, "bf16", True)
+    r256 = lambda x: -(-x // 256) * 256
+    assert 256 + r256(len(tiles) * 32) + r256(len(runs) * 16) > 8 << 20
+    (q, k, v), o, lse, keep = _buffers(n * ln, 2, 2, 128)
+    s = L.cpattn_fwd_static(big.handle, q, k, v, cp.DTYPE_BF16, 2, 2, 128, 0.1, 1, o, lse, None)
+    torch.cuda.synchronize()
     assert s == cp.WORKSPACE
     assert b"static scratch holds" in L.cpattn_last_error_string()
