@@ -23,6 +23,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <iterator>
 #include <numeric>
 
 #include "../../include/cpattn.h"
@@ -431,7 +432,77 @@ static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool cau
   std::vector<std::vector<Segment>> segs(cp);
   for (int r = 0; r < cp; ++r) segs[r] = segments_of(r);
 
-  const int r_lo = q_rank < 0 ? 0 : q_rank, r_hi = q_rank < 0 ? cp : q_rank + 1;
+  // The KV runs a query tile [qp_first, qp_last] of sequence `seq` owned by
+  // rank r reads at ring steps [s_lo, s_hi): at step st the pieces of rank
+  // (r - st) mod cp's shard of the sequence; runs in the future are dropped,
+  // runs crossing the diagonal are cut at the tile's last query and masked.
+  auto add_runs = [&](QTile* t, int r, int32_t seq, int64_t qp_first, int64_t qp_last, int s_lo, int s_hi) {
+    t->run_begin = (int32_t)wl->runs.size();
+    int64_t ntiles = 0;
+    for (int st = s_lo; st < s_hi; ++st) {
+      const int k = ((r - st) % cp + cp) % cp;
+      const auto rng = seq_range(segs[k], seq);
+      for (size_t i = rng.first; i < rng.second; ++i) {
+        const Segment& ks = segs[k][i];
+        KvRun run{};
+        run.kv_row0 = (int32_t)ks.row0;
+        run.kv_pos0 = (int32_t)ks.pos0;
+        int64_t len = ks.len;
+        run.causal = 0;
+        if (causal) {
+          if (ks.pos0 > qp_last) continue;                   // entirely in the future
+          if (ks.pos0 + ks.len - 1 > qp_first) {             // crosses the diagonal
+            len = std::min<int64_t>(ks.len, qp_last - ks.pos0 + 1);
+            run.causal = 1;
+          }
+        }
+        run.kv_len = (int32_t)len;
+        wl->runs.push_back(run);
+        ntiles += (len + tile_n - 1) / tile_n;
+      }
+    }
+    t->run_end = (int32_t)wl->runs.size();
+    if (pair) ntiles = (ntiles + 1) / 2;  // two pieces per kernel tile
+    t->n_kv_tiles = (int32_t)ntiles;
+    wl->total_kv_tiles += ntiles;
+  };
+
+  if (q_rank < 0 && !mesh && !gathered) {
+    // Whole call on global rows (zigzag, contiguous): a sequence's query rows
+    // are consecutive, so its tiles are cut from the sequence itself, ending
+    // at its last row (a partial tile falls at the start, where it sees the
+    // fewest keys), and a tile may hold the end of one chunk and the start of
+    // the next.  Each row still sees its own keys shard by shard: the tile
+    // walks the ring of the rank that owns its last row, and the position
+    // mask inside every run that crosses the tile's first query leaves each
+    // row exactly the pairs of its own ring steps.
+    std::vector<std::vector<std::pair<int64_t, int>>> owner(p.n_seqs);  // (pos0, rank) of each segment
+    std::vector<int64_t> base(p.n_seqs, -1), len(p.n_seqs, 0);
+    for (int r = 0; r < cp; ++r)
+      for (const Segment& qs : segs[r]) {
+        owner[qs.seq].push_back({qs.pos0, r});
+        base[qs.seq] = qs.row0 - qs.pos0;
+        len[qs.seq] += qs.len;
+      }
+    for (int32_t sq = 0; sq < p.n_seqs; ++sq) {
+      std::sort(owner[sq].begin(), owner[sq].end());
+      for (int64_t end = len[sq]; end > 0; end -= tile_m) {
+        const int64_t first = std::max<int64_t>(0, end - tile_m);
+        // the segment holding the last row: the last one starting at or before it
+        auto it = std::upper_bound(owner[sq].begin(), owner[sq].end(), std::make_pair(end - 1, cp));
+        const int r = std::prev(it)->second;
+        QTile t{};
+        t.q_row0 = (int32_t)(base[sq] + first);
+        t.q_pos0 = (int32_t)first;
+        t.q_rows = (int32_t)(end - first);
+        t.rank = r;
+        t.out_row0 = t.q_row0;
+        add_runs(&t, r, sq, first, end - 1, 0, cp);
+        wl->tiles.push_back(t);
+      }
+    }
+  }
+  const int r_lo = q_rank < 0 ? 0 : q_rank, r_hi = (q_rank < 0 ? (mesh || gathered ? cp : 0) : q_rank + 1);
   for (int r = r_lo; r < r_hi; ++r) {
     int64_t local = 0;  // rank-local row of the current segment
     for (const Segment& qs : segs[r]) {
@@ -446,36 +517,8 @@ static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool cau
           t.out_row0 = (int32_t)(local + off);  // partial outputs: rank-local rows
         else
           t.out_row0 = t.q_row0;                // global rows (gathered rows for GRID2D)
-        t.run_begin = (int32_t)wl->runs.size();
         const int64_t qp_first = qs.pos0 + off, qp_last = qp_first + rows - 1;
-        const int s_lo = q_rank < 0 ? 0 : step, s_hi = q_rank < 0 ? cp : step + 1;
-        int64_t ntiles = 0;
-        for (int st = s_lo; st < s_hi; ++st) {
-          const int k = ((r - st) % cp + cp) % cp;
-          const auto rng = seq_range(segs[k], qs.seq);
-          for (size_t i = rng.first; i < rng.second; ++i) {
-            const Segment& ks = segs[k][i];
-            KvRun run{};
-            run.kv_row0 = (int32_t)ks.row0;
-            run.kv_pos0 = (int32_t)ks.pos0;
-            int64_t len = ks.len;
-            run.causal = 0;
-            if (causal) {
-              if (ks.pos0 > qp_last) continue;                   // entirely in the future
-              if (ks.pos0 + ks.len - 1 > qp_first) {             // crosses the diagonal
-                len = std::min<int64_t>(ks.len, qp_last - ks.pos0 + 1);
-                run.causal = 1;
-              }
-            }
-            run.kv_len = (int32_t)len;
-            wl->runs.push_back(run);
-            ntiles += (len + tile_n - 1) / tile_n;
-          }
-        }
-        t.run_end = (int32_t)wl->runs.size();
-        if (pair) ntiles = (ntiles + 1) / 2;  // two pieces per kernel tile
-        t.n_kv_tiles = (int32_t)ntiles;
-        wl->total_kv_tiles += ntiles;
+        add_runs(&t, r, qs.seq, qp_first, qp_last, q_rank < 0 ? 0 : step, q_rank < 0 ? cp : step + 1);
         wl->tiles.push_back(t);
       }
       local += qs.len;

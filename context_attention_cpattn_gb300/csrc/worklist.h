@@ -1,9 +1,13 @@
 // Work-list records shared by the host planner and the attention kernels.
 //
-// A q tile is up to tile_m consecutive query rows of one sequence inside one
-// rank's shard.  Its KV runs list, in ring order, the key rows of the same
-// sequence that the tile's queries may see: at ring step t the q rank r reads
-// the shard of rank (r - t) mod cp, one run per contiguous piece of it.
+// A q tile is up to tile_m consecutive query rows of one sequence: inside one
+// rank's shard for a ring step, or, for a whole forward call on global rows,
+// cut from the sequence's end so that it may hold the end of one chunk and
+// the start of the next (owned then by the rank of its last row).  Its KV
+// runs list, in ring order, the key rows of the same sequence that the tile's
+// queries may see: at ring step t the q rank r reads the shard of rank
+// (r - t) mod cp, one run per contiguous piece of it; the position mask inside
+// a run leaves each row the pairs of its own ring steps.
 #pragma once
 
 #include <stdint.h>
@@ -22,7 +26,7 @@ typedef struct QTile {
   int32_t run_begin;  // KV runs [run_begin, run_end)
   int32_t run_end;
   int32_t n_kv_tiles; // sum over runs of ceil(kv_len / tile_n)
-  int32_t rank;       // virtual rank that owns the tile
+  int32_t rank;       // virtual rank that owns the tile (of its last row)
 } QTile;
 
 typedef struct KvRun {

@@ -226,7 +226,13 @@ cpattn_status_t cpattn_plan_get_a2a_map(const cpattn_plan_t* plan, int64_t* out,
  *     sequence (GRID2D, bidirectional only: the gathered row), count);
  *     out_row0 = output row of the first; runs
  *     [run_begin, run_end); pieces = kernel loop trips over its runs; rank =
- *     the virtual rank that owns the tile.
+ *     the virtual rank that owns the tile.  A tile of one ring step lies in
+ *     one chunk of its rank.  A tile of a whole forward call on global rows
+ *     (zigzag, contiguous) is cut from its sequence, ending at the
+ *     sequence's last row, up to the kernel's tile height, so it may hold
+ *     the end of one chunk and the start of the next; its rank owns its last
+ *     row and its runs follow that rank's ring, with the position mask in
+ *     every run that crosses the tile's first query.
  *   run: row0, pos0, len = rows of the other side; masked = 1 when the
  *     position mask (key position <= query position) applies inside the run,
  *     0 when every pair of the tile and the run is allowed.
