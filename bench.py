@@ -47,9 +47,12 @@ METRIC = "packed varlen attention fwd TFLOP/s (valid tokens) and % of GB300 BF16
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "dynamic_cp_microbatch"
 FALLBACK_BF16_TFLOPS = 1900.0
-TC_SOURCES = ("context_attention_cpattn_gb300/csrc/attn_tc.cu", "context_attention_cpattn_gb300/csrc/common.cuh")
+# a kernel's DRAM traffic depends on its source and on the work list the planner hands it
+TC_SOURCES = ("context_attention_cpattn_gb300/csrc/attn_tc.cu", "context_attention_cpattn_gb300/csrc/common.cuh",
+              "context_attention_cpattn_gb300/csrc/plan.cpp")
 TRAFFIC_FILE = "profiles/traffic.json"
-BWD_SOURCES = ("context_attention_cpattn_gb300/csrc/attn_bwd_tc.cu", "context_attention_cpattn_gb300/csrc/common.cuh")
+BWD_SOURCES = ("context_attention_cpattn_gb300/csrc/attn_bwd_tc.cu", "context_attention_cpattn_gb300/csrc/common.cuh",
+               "context_attention_cpattn_gb300/csrc/plan.cpp")
 
 
 def parse_args(argv=None):

@@ -561,8 +561,73 @@ static std::shared_ptr<WorkList> build_worklist_bwd(const cpattn_plan_t& p, bool
       if (b > a) segs[r].push_back({a, b - a, 0, a});
     }
   }
+  // The query runs a KV tile [kp_first, kp_last] of sequence `seq` meets at
+  // the q ranks `q_ranks` (in ring order): queries before the tile's first
+  // key see none of it; runs with a query before the tile's last key are
+  // masked.
+  auto add_runs = [&](QTile* t, const std::vector<int>& q_ranks, int32_t seq, int64_t kp_first, int64_t kp_last) {
+    t->run_begin = (int32_t)wl->runs.size();
+    int64_t pieces = 0;
+    for (int r : q_ranks) {
+      const auto rng = seq_range(segs[r], seq);
+      for (size_t i = rng.first; i < rng.second; ++i) {
+        const Segment& qs = segs[r][i];
+        int64_t q0 = qs.pos0, q1 = qs.pos0 + qs.len;  // query positions [q0, q1)
+        KvRun run{};
+        run.causal = 0;
+        if (causal) {
+          if (q1 - 1 < kp_first) continue;         // every query precedes the tile
+          q0 = std::max<int64_t>(q0, kp_first);    // queries before the first key see nothing
+          if (q0 < kp_last) run.causal = 1;        // some query precedes some key
+        }
+        run.kv_row0 = (int32_t)(qs.row0 + (q0 - qs.pos0));
+        run.kv_pos0 = (int32_t)q0;
+        run.kv_len = (int32_t)(q1 - q0);
+        wl->runs.push_back(run);
+        pieces += (run.kv_len + tile_q - 1) / tile_q;
+      }
+    }
+    t->run_end = (int32_t)wl->runs.size();
+    t->n_kv_tiles = (int32_t)pieces;
+    wl->total_kv_tiles += pieces;
+  };
+
+  if (q_rank < 0 && !gathered) {
+    // Whole call on global rows (zigzag, contiguous): KV tiles are cut from
+    // each sequence from its first row on (a partial tile falls at the end,
+    // where the fewest queries see it), so a tile may hold the end of one
+    // chunk and the start of the next.  It is owned by the rank of its first
+    // key and meets the q ranks of that rank's ring; the position mask leaves
+    // each key the queries of its own ring steps.
+    std::vector<std::vector<std::pair<int64_t, int>>> owner(p.n_seqs);  // (pos0, rank) of each segment
+    std::vector<int64_t> base(p.n_seqs, -1), len(p.n_seqs, 0);
+    for (int r = 0; r < cp; ++r)
+      for (const Segment& ks : segs[r]) {
+        owner[ks.seq].push_back({ks.pos0, r});
+        base[ks.seq] = ks.row0 - ks.pos0;
+        len[ks.seq] += ks.len;
+      }
+    std::vector<int> q_ranks(cp);
+    for (int32_t sq = 0; sq < p.n_seqs; ++sq) {
+      std::sort(owner[sq].begin(), owner[sq].end());
+      for (int64_t first = 0; first < len[sq]; first += tile_k) {
+        const int64_t last = std::min<int64_t>(len[sq], first + tile_k) - 1;
+        auto it = std::upper_bound(owner[sq].begin(), owner[sq].end(), std::make_pair(first, cp));
+        const int k = std::prev(it)->second;
+        QTile t{};
+        t.q_row0 = (int32_t)(base[sq] + first);
+        t.q_pos0 = (int32_t)first;
+        t.q_rows = (int32_t)(last - first + 1);
+        t.out_row0 = t.q_row0;
+        t.rank = k;
+        for (int tt = 0; tt < cp; ++tt) q_ranks[tt] = (k + tt) % cp;
+        add_runs(&t, q_ranks, sq, first, last);
+        wl->tiles.push_back(t);
+      }
+    }
+  }
   // KV ranks to visit, each with the ring steps (q ranks) that read it
-  for (int k = 0; k < cp; ++k) {
+  for (int k = 0; k < (q_rank < 0 && !gathered ? 0 : cp); ++k) {
     std::vector<int> q_ranks;
     if (q_rank < 0) {
       for (int t = 0; t < cp; ++t) q_ranks.push_back((k + t) % cp);
@@ -579,31 +644,8 @@ static std::shared_ptr<WorkList> build_worklist_bwd(const cpattn_plan_t& p, bool
         t.q_rows = (int32_t)rows;
         t.out_row0 = t.q_row0;
         t.rank = k;
-        t.run_begin = (int32_t)wl->runs.size();
         const int64_t kp_first = ks.pos0 + off, kp_last = kp_first + rows - 1;
-        int64_t pieces = 0;
-        for (int r : q_ranks) {
-          const auto rng = seq_range(segs[r], ks.seq);
-          for (size_t i = rng.first; i < rng.second; ++i) {
-            const Segment& qs = segs[r][i];
-            int64_t q0 = qs.pos0, q1 = qs.pos0 + qs.len;  // query positions [q0, q1)
-            KvRun run{};
-            run.causal = 0;
-            if (causal) {
-              if (q1 - 1 < kp_first) continue;         // every query precedes the tile
-              q0 = std::max<int64_t>(q0, kp_first);    // queries before the first key see nothing
-              if (q0 < kp_last) run.causal = 1;        // some query precedes some key
-            }
-            run.kv_row0 = (int32_t)(qs.row0 + (q0 - qs.pos0));
-            run.kv_pos0 = (int32_t)q0;
-            run.kv_len = (int32_t)(q1 - q0);
-            wl->runs.push_back(run);
-            pieces += (run.kv_len + tile_q - 1) / tile_q;
-          }
-        }
-        t.run_end = (int32_t)wl->runs.size();
-        t.n_kv_tiles = (int32_t)pieces;
-        wl->total_kv_tiles += pieces;
+        add_runs(&t, q_ranks, ks.seq, kp_first, kp_last);
         wl->tiles.push_back(t);
       }
     }

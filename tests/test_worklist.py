@@ -8,9 +8,10 @@ position <= query position ("Scaling video training with parallelism",
 section 2: blockwise attention over the KV blocks of the ring), or the
 teacher-forcing mask for paired plans.  Also checked: every query (forward)
 or key (backward) row lies in exactly one tile, tiles hold consecutive
-positions of one sequence owned by one rank (whole forward calls on global
-rows: tiles cut from the sequence's end, owned by the rank of their last
-row), runs are in ring order (rank (r - t) mod cp at step t forward,
+positions of one sequence owned by one rank (whole calls on global rows:
+query tiles cut from the sequence's end and owned by the rank of their last
+row, KV tiles cut from its start and owned by the rank of their first key),
+runs are in ring order (rank (r - t) mod cp at step t forward,
 (k + t) mod cp backward), the per-tile piece counts the kernels loop over,
 longest-first order, and the rank-local output rows of one ring step."""
 
@@ -64,7 +65,7 @@ def replay(tiles, runs, tok_of_row, seq, pos, causal, tile_rows, piece, backward
     (bidirectional only), where they are the gathered rows."""
     T = len(seq)
     row_pos = np.arange(len(tok_of_row)) if gathered else pos[tok_of_row]
-    packed = not backward and q_rank is None and not gathered and rank_of_tok is not None
+    packed = q_rank is None and not gathered and rank_of_tok is not None
     seq_len = np.bincount(seq)
     count = np.zeros((T, T), dtype=np.int32)
     seen = np.zeros(T, dtype=np.int32)
@@ -74,13 +75,18 @@ def replay(tiles, runs, tok_of_row, seq, pos, causal, tile_rows, piece, backward
         tt = tok_of_row[row0:row0 + rows]
         assert (seq[tt] == seq[tt[0]]).all() and (row_pos[row0:row0 + rows] == pos0 + np.arange(rows)).all()
         seen[tt] += 1
-        if packed:
-            # a whole forward call on global rows: tiles are cut from the
+        if packed and not backward:
+            # a whole forward call on global rows: query tiles are cut from the
             # sequence, ending at its last row, and owned by the rank of their
             # last row (they may hold the end of one chunk and the start of
             # the next)
             assert rank_of_tok[tt[-1]] == rank
             assert (seq_len[seq[tt[0]]] - (pos0 + rows)) % tile_rows == 0 and (rows == tile_rows or pos0 == 0)
+        elif packed:
+            # the backward's KV tiles: cut from the sequence's first row on,
+            # owned by the rank of their first key
+            assert rank_of_tok[tt[0]] == rank
+            assert pos0 % tile_rows == 0 and (rows == tile_rows or pos0 + rows == seq_len[seq[tt[0]]])
         elif rank_of_tok is not None:
             assert (rank_of_tok[tt] == rank).all()
             if q_rank is not None:
