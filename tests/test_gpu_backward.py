@@ -241,12 +241,12 @@ def _full_size_single_sequence(cp, name, n_rows):
 
 
 def test_long_video_200k_backward_full_size(cp):
-    _full_size_single_sequence(cp, "long_video_200k_gqa", 192)
+    _full_size_single_sequence(cp, "long_video_200k_gqa", 1024)
 
 
 def test_video_latent_grid2d_backward_full_size(cp):
-    _full_size_single_sequence(cp, "video_latent_grid2d", 256)
+    _full_size_single_sequence(cp, "video_latent_grid2d", 2048)
 
 
 def test_single_seq_1m_backward_full_size(cp):
-    _full_size_single_sequence(cp, "single_seq_1m_gqa", 24)
+    _full_size_single_sequence(cp, "single_seq_1m_gqa", 256)
