@@ -555,6 +555,8 @@ static cpattn_status_t run_attention(const cpattn_plan_t* cplan, const void* q, 
   a.tiles = reinterpret_cast<const QTile*>(ws + L.tiles);
   a.runs = reinterpret_cast<const KvRun*>(ws + L.runs);
   a.n_tiles = (int32_t)wl->tiles.size();
+  a.total_pieces = wl->total_kv_tiles;
+  a.max_pieces = wl->tiles.empty() ? 0 : wl->tiles.front().n_kv_tiles;  // longest first
   a.o = o;
   a.lse = lse;
   a.ws = reinterpret_cast<WsHeader*>(ws);

@@ -58,6 +58,10 @@ namespace cpattn {
 
 using namespace dev;
 
+// Cap on the keys and values of one group of KV heads, about the size of L2
+// (129 MB): larger groups lose the L2 reuse of head-by-head order.
+constexpr int64_t kKvGroupBytes = 144ll << 20;
+
 struct alignas(64) TcParams {
   CUtensorMap tm_q;
   CUtensorMap tm_k;
@@ -71,6 +75,7 @@ struct alignas(64) TcParams {
   int64_t lse_ld;
   int32_t n_tiles;
   int32_t H, Hkv;
+  int32_t kv_group;   // KV heads per item group (divides Hkv)
   float scale;        // softmax scale (natural-log domain)
   float scale_log2;   // scale * log2(e)
   float thresh_raw;   // 8 / scale_log2: raw-score growth that forces a rescale
@@ -120,13 +125,20 @@ struct PieceCursor {
 struct Item {
   int tile_id, h, g;
 };
-__device__ __forceinline__ Item item_of(int i, int n_tiles, int G) {
+// Items run in groups of kv_group KV heads; inside a group, tile by tile in
+// the work list's longest-first order, each tile for every query head of the
+// group.  A group's keys and values stay in L2 while its tiles run, and the
+// last group ends on its shortest tiles.
+__device__ __forceinline__ Item item_of(int i, int n_tiles, int G, int kv_group) {
   Item it;
-  const int hq = i % G;
-  const int rest = i / G;
-  it.tile_id = rest % n_tiles;
-  it.g = rest / n_tiles;
-  it.h = it.g * G + hq;
+  const int span = kv_group * G;  // query heads per group
+  const int per_group = n_tiles * span;
+  const int grp = i / per_group;
+  const int r = i - grp * per_group;
+  it.tile_id = r / span;
+  const int w = r - it.tile_id * span;
+  it.g = grp * kv_group + w / G;
+  it.h = it.g * G + w % G;
   return it;
 }
 
@@ -224,7 +236,7 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
         item_ring[k & 3] = (i < n_items) ? i : -1;
         mbar_arrive(item_full + (k & 3));
         if (i >= n_items) break;
-        const Item it = item_of(i, p.n_tiles, G);
+        const Item it = item_of(i, p.n_tiles, G, p.kv_group);
         const QTile tile = p.tiles[it.tile_id];
         i = (int)gridDim.x + (int)atomicAdd(&p.ws->next_item, 1u);
         if (tile.n_kv_tiles == 0) continue;
@@ -274,7 +286,7 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
       for (int k = 0; ok; ++k) {
         const int i = take_item(k, 5);
         if (i < 0) break;
-        const int n_kv = p.tiles[item_of(i, p.n_tiles, G).tile_id].n_kv_tiles;
+        const int n_kv = p.tiles[item_of(i, p.n_tiles, G, p.kv_group).tile_id].n_kv_tiles;
         if (n_kv == 0) continue;
         if (!wait_bounded(q_full, qc & 1, abort_flag, p.ws, 6, wait_ns)) break;
         ++qc;
@@ -310,7 +322,7 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
       for (int k = 0; ok; ++k) {
         const int i = take_item(k, 19);
         if (i < 0) break;
-        const int n_kv = p.tiles[item_of(i, p.n_tiles, G).tile_id].n_kv_tiles;
+        const int n_kv = p.tiles[item_of(i, p.n_tiles, G, p.kv_group).tile_id].n_kv_tiles;
         if (n_kv == 0) continue;
         for (int j = 0; j < n_kv; ++j, ++g) {
           const int b = g & 1;
@@ -345,7 +357,7 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
       const int i = take_item(k, 12);
       if (!__all_sync(0xffffffffu, i != -2)) break;
       if (i < 0) break;
-      const Item it = item_of(i, p.n_tiles, G);
+      const Item it = item_of(i, p.n_tiles, G, p.kv_group);
       const QTile tile = p.tiles[it.tile_id];
       const int n_kv = tile.n_kv_tiles;
       const int q_pos = tile.q_pos0 + row;
@@ -538,6 +550,19 @@ cudaError_t launch_attn_bf16_tc(const AttnArgs& a, std::string* err) {
   }
   // persistent blocks, two per SM, each walking items blockIdx.x, +gridDim.x, ...
   const int64_t blocks = std::min<int64_t>(items, 2 * (int64_t)num_sms());
+  // Item groups: the smallest divisor of Hkv whose work per block is at least
+  // 1.25 times the longest item, so that the last group's longest items do
+  // not run alone at the end, as long as the group's K and V fit the budget;
+  // past the budget, the largest divisor that fits.
+  p.kv_group = 1;
+  const int64_t kv_head_bytes = 2 * (int64_t)a.kv_rows_total * a.D * 2;
+  const int G = a.H / a.Hkv;
+  for (int d = 1; d <= a.Hkv; ++d) {
+    if (a.Hkv % d != 0) continue;
+    if (d > 1 && d * kv_head_bytes > kKvGroupBytes) break;
+    p.kv_group = d;
+    if (4 * (int64_t)d * G * a.total_pieces >= 5 * (int64_t)a.max_pieces * blocks) break;
+  }
   if (a.D == 128) return a.partial ? launch_tc<128, true>(p, (int)blocks, a.stream)
                                    : launch_tc<128, false>(p, (int)blocks, a.stream);
   return a.partial ? launch_tc<64, true>(p, (int)blocks, a.stream) : launch_tc<64, false>(p, (int)blocks, a.stream);

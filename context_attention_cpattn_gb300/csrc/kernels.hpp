@@ -24,6 +24,8 @@ struct AttnArgs {
   const QTile* tiles = nullptr;  // device
   const KvRun* runs = nullptr;   // device
   int32_t n_tiles = 0;
+  int64_t total_pieces = 0;      // KV pieces over all tiles (one head's work)
+  int32_t max_pieces = 0;        // KV pieces of the longest tile
   void* o = nullptr;             // final: dtype [*,H,D] at global rows; partial: fp32 [*,H,D]
   bool partial = false;
   float* lse = nullptr;          // [H, lse_ld]

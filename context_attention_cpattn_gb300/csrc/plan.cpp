@@ -339,6 +339,21 @@ bool ring_entry(const cpattn_plan_t& p, int r, int t, bool causal, int32_t* kv_r
   return true;
 }
 
+// Appends a run to a tile's list; a run that continues the previous run of
+// the same ring step (the next rows and positions of the same shard) is
+// merged into it, masked if either part is.
+static void append_run(WorkList* wl, size_t step_begin, const KvRun& run) {
+  if (wl->runs.size() > step_begin) {
+    KvRun& prev = wl->runs.back();
+    if (prev.kv_row0 + prev.kv_len == run.kv_row0 && prev.kv_pos0 + prev.kv_len == run.kv_pos0) {
+      prev.kv_len += run.kv_len;
+      prev.causal |= run.causal;
+      return;
+    }
+  }
+  wl->runs.push_back(run);
+}
+
 // Segments of `rank` that belong to sequence `seq` (segments are ordered by sequence).
 static std::pair<size_t, size_t> seq_range(const std::vector<Segment>& segs, int32_t seq) {
   auto lo = std::lower_bound(segs.begin(), segs.end(), seq,
@@ -438,10 +453,10 @@ static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool cau
   // runs crossing the diagonal are cut at the tile's last query and masked.
   auto add_runs = [&](QTile* t, int r, int32_t seq, int64_t qp_first, int64_t qp_last, int s_lo, int s_hi) {
     t->run_begin = (int32_t)wl->runs.size();
-    int64_t ntiles = 0;
     for (int st = s_lo; st < s_hi; ++st) {
       const int k = ((r - st) % cp + cp) % cp;
       const auto rng = seq_range(segs[k], seq);
+      const size_t step_begin = wl->runs.size();
       for (size_t i = rng.first; i < rng.second; ++i) {
         const Segment& ks = segs[k][i];
         KvRun run{};
@@ -457,11 +472,12 @@ static std::shared_ptr<WorkList> build_worklist(const cpattn_plan_t& p, bool cau
           }
         }
         run.kv_len = (int32_t)len;
-        wl->runs.push_back(run);
-        ntiles += (len + tile_n - 1) / tile_n;
+        append_run(wl.get(), step_begin, run);
       }
     }
     t->run_end = (int32_t)wl->runs.size();
+    int64_t ntiles = 0;
+    for (int32_t i = t->run_begin; i < t->run_end; ++i) ntiles += (wl->runs[i].kv_len + tile_n - 1) / tile_n;
     if (pair) ntiles = (ntiles + 1) / 2;  // two pieces per kernel tile
     t->n_kv_tiles = (int32_t)ntiles;
     wl->total_kv_tiles += ntiles;
@@ -567,9 +583,9 @@ static std::shared_ptr<WorkList> build_worklist_bwd(const cpattn_plan_t& p, bool
   // masked.
   auto add_runs = [&](QTile* t, const std::vector<int>& q_ranks, int32_t seq, int64_t kp_first, int64_t kp_last) {
     t->run_begin = (int32_t)wl->runs.size();
-    int64_t pieces = 0;
     for (int r : q_ranks) {
       const auto rng = seq_range(segs[r], seq);
+      const size_t step_begin = wl->runs.size();
       for (size_t i = rng.first; i < rng.second; ++i) {
         const Segment& qs = segs[r][i];
         int64_t q0 = qs.pos0, q1 = qs.pos0 + qs.len;  // query positions [q0, q1)
@@ -583,11 +599,12 @@ static std::shared_ptr<WorkList> build_worklist_bwd(const cpattn_plan_t& p, bool
         run.kv_row0 = (int32_t)(qs.row0 + (q0 - qs.pos0));
         run.kv_pos0 = (int32_t)q0;
         run.kv_len = (int32_t)(q1 - q0);
-        wl->runs.push_back(run);
-        pieces += (run.kv_len + tile_q - 1) / tile_q;
+        append_run(wl.get(), step_begin, run);
       }
     }
     t->run_end = (int32_t)wl->runs.size();
+    int64_t pieces = 0;
+    for (int32_t i = t->run_begin; i < t->run_end; ++i) pieces += (wl->runs[i].kv_len + tile_q - 1) / tile_q;
     t->n_kv_tiles = (int32_t)pieces;
     wl->total_kv_tiles += pieces;
   };

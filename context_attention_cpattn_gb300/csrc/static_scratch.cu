@@ -121,6 +121,8 @@ extern "C" cpattn_status_t cpattn_fwd_static(const cpattn_plan_t* cplan, const v
   a.tiles = reinterpret_cast<const cpattn::QTile*>(base + off_tiles);
   a.runs = reinterpret_cast<const cpattn::KvRun*>(base + off_runs);
   a.n_tiles = (int32_t)wl->tiles.size();
+  a.total_pieces = wl->total_kv_tiles;
+  a.max_pieces = wl->tiles.empty() ? 0 : wl->tiles.front().n_kv_tiles;  // longest first
   a.o = o;
   a.partial = false;
   a.lse = lse;
