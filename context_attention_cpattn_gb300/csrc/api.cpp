@@ -703,6 +703,8 @@ static cpattn_status_t run_backward(const cpattn_plan_t* cplan, const void* q, c
   a.tiles = reinterpret_cast<const QTile*>(ws + WL.tiles);
   a.runs = reinterpret_cast<const KvRun*>(ws + WL.runs);
   a.n_tiles = (int32_t)wl->tiles.size();
+  a.total_pieces = wl->total_kv_tiles;
+  a.max_pieces = wl->tiles.empty() ? 0 : wl->tiles.front().n_kv_tiles;  // longest first
   a.nl2 = reinterpret_cast<float*>(ws + L.nl2);
   a.nd = reinterpret_cast<float*>(ws + L.nd);
   a.ws = reinterpret_cast<WsHeader*>(ws);

@@ -66,6 +66,10 @@ using namespace dev;
 
 namespace {
 
+// Cap on the queries, dO and fp32 dQ of one group of KV heads, about the
+// size of L2 (129 MB): larger groups lose the L2 reuse of head-by-head order.
+constexpr int64_t kQGroupBytes = 144ll << 20;
+
 struct alignas(64) BwdParams {
   CUtensorMap tm_k, tm_v;   // [rows, Hkv, D], 128-row boxes
   CUtensorMap tm_q, tm_do;  // [rows, H, D], 64-row boxes
@@ -80,6 +84,7 @@ struct alignas(64) BwdParams {
   const int64_t* out_map;   // optional: output row of a buffer row
   WsHeader* ws;
   int32_t n_tiles, H, Hkv;
+  int32_t kv_group;         // KV heads per item group (divides Hkv)
   float scale_log2;         // softmax scale * log2(e)
   float scale;              // softmax scale (dS is scaled by it)
 };
@@ -136,7 +141,15 @@ struct QCursor {
 struct Item {
   int tile_id, g;
 };
-__device__ __forceinline__ Item item_of(int i, int n_tiles) { return Item{i % n_tiles, i / n_tiles}; }
+// Items run in groups of kv_group KV heads; inside a group, KV tile by KV
+// tile in the work list's longest-first order, each tile for every KV head of
+// the group (the group's queries, dO and dQ stay in L2 while it runs).
+__device__ __forceinline__ Item item_of(int i, int n_tiles, int kv_group) {
+  const int per_group = n_tiles * kv_group;
+  const int grp = i / per_group;
+  const int r = i - grp * per_group;
+  return Item{r / kv_group, grp * kv_group + r % kv_group};
+}
 
 template <int D, bool kAccum>
 __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_constant__ BwdParams p) {
@@ -250,7 +263,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
         mbar_arrive(item_full + (k & 3));
       }
       if (i >= n_items) break;
-      const Item it = item_of(i, p.n_tiles);
+      const Item it = item_of(i, p.n_tiles, p.kv_group);
       const QTile tile = p.tiles[it.tile_id];
       int nxt = 0;
       if (lane == 0) nxt = (int)gridDim.x + (int)atomicAdd(&p.ws->next_item, 1u);
@@ -323,7 +336,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
       for (int k = 0; ok; ++k) {
         const int i = take_item(k, 5);
         if (i < 0) break;
-        const int n = p.tiles[item_of(i, p.n_tiles).tile_id].n_kv_tiles * G;
+        const int n = p.tiles[item_of(i, p.n_tiles, p.kv_group).tile_id].n_kv_tiles * G;
         if (n == 0) continue;
         ok = wait_bounded(kv_full, kc & 1, abort_flag, p.ws, 6);
         if (!ok) break;
@@ -359,7 +372,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
       const int i = take_item(k, 13);
       if (!__all_sync(0xffffffffu, i != -2)) break;
       if (i < 0) break;
-      const Item it = item_of(i, p.n_tiles);
+      const Item it = item_of(i, p.n_tiles, p.kv_group);
       const QTile tile = p.tiles[it.tile_id];
       const int n = tile.n_kv_tiles * G;
       const bool key_ok = row < tile.q_rows;
@@ -509,7 +522,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
       const int i = take_item(k, 19);
       if (!__all_sync(0xffffffffu, i != -2)) break;
       if (i < 0) break;
-      const Item it = item_of(i, p.n_tiles);
+      const Item it = item_of(i, p.n_tiles, p.kv_group);
       const QTile tile = p.tiles[it.tile_id];
       const int n = tile.n_kv_tiles * G;
       QCursor cur{tile.run_begin, 0, tile.run_begin, tile.run_end, 0};
@@ -567,7 +580,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
       for (int k = 0; ok; ++k) {
         const int i = take_item(k, 24);
         if (i < 0) break;
-        const int n = p.tiles[item_of(i, p.n_tiles).tile_id].n_kv_tiles * G;
+        const int n = p.tiles[item_of(i, p.n_tiles, p.kv_group).tile_id].n_kv_tiles * G;
         if (n == 0) continue;
         for (int t = 0; ok && t < n; ++t, ++g) {
           const int b = g & 1;
@@ -776,6 +789,18 @@ cudaError_t launch_attn_bwd_bf16_tc(const BwdArgs& a, std::string* err) {
     return cudaErrorInvalidValue;
   }
   const int64_t blocks = std::min<int64_t>(items, (int64_t)num_sms());
+  // Item groups: the smallest divisor of Hkv whose work per block is at least
+  // 1.25 times the longest item, so that the last group's longest items do
+  // not run alone at the end, as long as the group's Q, dO and fp32 dQ fit
+  // about one L2; past that, the largest divisor that fits.
+  p.kv_group = 1;
+  const int64_t q_side_bytes = (int64_t)(a.H / a.Hkv) * a.rows_total * a.D * (2 + 2 + 4);
+  for (int d = 1; d <= a.Hkv; ++d) {
+    if (a.Hkv % d != 0) continue;
+    if (d > 1 && d * q_side_bytes > kQGroupBytes) break;
+    p.kv_group = d;
+    if (4 * (int64_t)d * a.total_pieces >= 5 * (int64_t)a.max_pieces * blocks) break;
+  }
   return a.accumulate ? launch_bwd_tc<128, true>(p, (int)blocks, a.stream)
                       : launch_bwd_tc<128, false>(p, (int)blocks, a.stream);
 }

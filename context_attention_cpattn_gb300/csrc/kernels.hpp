@@ -63,6 +63,8 @@ struct BwdArgs {
   const QTile* tiles = nullptr;     // device
   const KvRun* runs = nullptr;      // device
   int32_t n_tiles = 0;
+  int64_t total_pieces = 0;      // query pieces over all KV tiles (one KV head's work per query head)
+  int32_t max_pieces = 0;        // query pieces of the longest KV tile
   float* nl2 = nullptr;             // scratch [H, rows_total]: -lse*log2(e)
   float* nd = nullptr;              // scratch [H, rows_total]: -rowsum(dO*O)
   float* dq_acc = nullptr;          // fp32 [rows_total, H, D] at buffer rows, accumulated
