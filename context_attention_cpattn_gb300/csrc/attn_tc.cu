@@ -38,7 +38,10 @@
 //               kept: O and the sum share it, so the final O/l is exact).  A
 //               rescale first waits for PV_{j-1}.  After an item's last PV they
 //               read O, release it for the next item's first PV, and write O/l
-//               and the LSE at the output rows.
+//               and the LSE at the output rows: a warp whose 32 rows are all
+//               valid (bf16 final outputs at contiguous rows) stages them 64
+//               columns at a time in shared memory and writes them with one
+//               tensor store, the others store row by row.
 //
 // Shared-memory operand layouts (1024-byte aligned, SWIZZLE_128B):
 //   Q:    [128 rows][64 columns] boxes, K-major.
@@ -66,6 +69,7 @@ struct alignas(64) TcParams {
   CUtensorMap tm_q;
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  CUtensorMap tm_o;   // bf16 O [rows, H, D], 64 columns x 1 head x 32 rows boxes (when o_tma)
   const QTile* tiles;
   const KvRun* runs;
   void* o;
@@ -76,6 +80,7 @@ struct alignas(64) TcParams {
   int32_t n_tiles;
   int32_t H, Hkv;
   int32_t kv_group;   // KV heads per item group (divides Hkv)
+  int32_t o_tma;      // 1: full 32-row slices of O leave through tm_o
   float scale;        // softmax scale (natural-log domain)
   float scale_log2;   // scale * log2(e)
   float thresh_raw;   // 8 / scale_log2: raw-score growth that forces a rescale
@@ -92,7 +97,14 @@ struct TcCfg {
   static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;  // V[2]
   static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + 256;  // 29 mbarriers (232 bytes) fit below
-  static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;  // + alignment slack
+  // O staging for the epilogue's tensor stores: per softmax warp 32 rows x 64
+  // columns of bf16 (128-byte swizzled rows), at the next 1024-byte boundary
+  static constexpr uint32_t OFF_STG = (OFF_MISC + 64 + 1023) / 1024 * 1024;
+  static constexpr uint32_t STG_WARP = 32 * 128;
+  // No alignment slack: where the dynamic shared memory does not start on a
+  // 1024-byte boundary, the layout shifts up by the padding, the staging area
+  // no longer fits and the epilogue stores O row by row instead.
+  static constexpr uint32_t SMEM = OFF_STG + 4 * STG_WARP;
   static constexpr uint32_t TMEM_COLS = 256;              // S0 | S1 | O
   static constexpr uint32_t TM_S = 0, TM_O = 128;         // S buffer b at TM_S + 64 b
 };
@@ -149,7 +161,10 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
   constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t smem_pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + smem_pad;
+  static_assert(C::OFF_MISC + 64 + 1023 <= C::SMEM, "the layout without staging must fit any padding");
+  const bool staged = p.o_tma && smem_pad == 0;  // the staging area lies inside the allocation
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
@@ -454,41 +469,80 @@ __global__ void __launch_bounds__(224, 2) attn_fwd_tc_kernel(const __grid_consta
       const float inv_l = has ? 1.f / l : 0.f;
       const int64_t out_row = p.out_map ? p.out_map[tile.out_row0 + (valid_row ? row : 0)]
                                         : (int64_t)tile.out_row0 + row;
+      if (!kPartial && staged && n_kv > 0 && quad * 32 + 32 <= tile.q_rows) {
+        // All 32 rows of this warp are valid: O leaves 64 columns at a time
+        // through the warp's staging slice and one tensor store, which writes
+        // whole lines instead of 16 bytes of 32 rows per store instruction.
+        uint8_t* stg = smem + C::OFF_STG + quad * C::STG_WARP;
 #pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
-        uint32_t o[32];
-        if (n_kv > 0) {
-          tmem_ld32_wait(tl + C::TM_O + 32u * cb, o);
-          if (cb == D / 32 - 1) {
-            // O has been read: the next item's first PV may overwrite it
-            tc_fence_before();
-            mbar_arrive(o_free);
+        for (int hf = 0; hf < D / 64; ++hf) {
+          uint32_t pk[32];  // 64 columns of this row as bf16 pairs
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t o[32];
+            tmem_ld32_wait(tl + C::TM_O + 64u * hf + 32u * cc, o);
+            if (hf == D / 64 - 1 && cc == 1) {
+              // O has been read: the next item's first PV may overwrite it
+              tc_fence_before();
+              mbar_arrive(o_free);
+            }
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              pk[16 * cc + q] = pack_bf16x2(has ? __uint_as_float(o[2 * q]) * inv_l : 0.f,
+                                            has ? __uint_as_float(o[2 * q + 1]) * inv_l : 0.f);
           }
-        } else {
+          // the slice is free once the previous tensor store has read it
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+          const uint32_t row_addr = smem_u32(stg) + lane * 128;
 #pragma unroll
-          for (int q = 0; q < 32; ++q) o[q] = 0u;
+          for (int c = 0; c < 8; ++c)  // 16-byte chunk c of the row, 128-byte swizzle
+            st_shared_v4(row_addr + ((c ^ (lane & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&p.tm_o, stg, 64 * hf, it.h, (int)out_row);
+            bulk_commit_group();
+          }
         }
-        if (valid_row) {
-          float v[32];
+      } else {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] = has ? __uint_as_float(o[q]) * inv_l : 0.f;
-          if (kPartial) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + (out_row * p.H + it.h) * D + 32 * cb);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t o[32];
+          if (n_kv > 0) {
+            tmem_ld32_wait(tl + C::TM_O + 32u * cb, o);
+            if (cb == D / 32 - 1) {
+              // O has been read: the next item's first PV may overwrite it
+              tc_fence_before();
+              mbar_arrive(o_free);
+            }
           } else {
-            uint4* dst =
-                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (out_row * p.H + it.h) * D + 32 * cb);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                  pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+            for (int q = 0; q < 32; ++q) o[q] = 0u;
+          }
+          if (valid_row) {
+            float v[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = has ? __uint_as_float(o[q]) * inv_l : 0.f;
+            if (kPartial) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + (out_row * p.H + it.h) * D + 32 * cb);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+              uint4* dst =
+                  reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + (out_row * p.H + it.h) * D + 32 * cb);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                    pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+            }
           }
         }
       }
       if (valid_row) p.lse[(int64_t)it.h * p.lse_ld + out_row] = has ? m_ref * p.scale + logf(l) : -INFINITY;
       if (n_kv > 0) ++oc;
     }
+    if (lane == 0) bulk_wait_group_all();  // this warp's tensor stores of O have completed
   }
 
   // ------------------------------------------------------------ teardown
@@ -517,6 +571,9 @@ static cudaError_t launch_tc(const TcParams& p, int n_blocks, cudaStream_t strea
   auto kern = attn_fwd_tc_kernel<D, kPartial>;
   const uint32_t smem = TcCfg<D>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // two blocks per SM take the whole shared-memory carve-out
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   kern<<<n_blocks, 224, smem, stream>>>(p);
   return cudaGetLastError();
@@ -529,6 +586,11 @@ cudaError_t launch_attn_bf16_tc(const AttnArgs& a, std::string* err) {
       !make_tensor_map_bf16(&p.tm_k, a.k, a.kv_rows_total, a.Hkv, a.D, 64, err) ||
       !make_tensor_map_bf16(&p.tm_v, a.v, a.kv_rows_total, a.Hkv, a.D, 64, err))
     return cudaErrorInvalidValue;
+  if (!a.partial && !a.out_map) {
+    // final outputs at contiguous rows: full 32-row slices leave by tensor stores
+    if (!make_tensor_map_bf16(&p.tm_o, a.o, a.q_rows_total, a.H, a.D, 32, err)) return cudaErrorInvalidValue;
+    p.o_tma = 1;
+  }
   p.tiles = a.tiles;
   p.runs = a.runs;
   p.o = a.o;
