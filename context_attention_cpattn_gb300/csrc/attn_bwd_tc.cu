@@ -74,6 +74,7 @@ struct alignas(64) BwdParams {
   CUtensorMap tm_k, tm_v;   // [rows, Hkv, D], 128-row boxes
   CUtensorMap tm_q, tm_do;  // [rows, H, D], 64-row boxes
   CUtensorMap tm_dq;        // fp32 dQ accumulator [rows, H, D], 64-row boxes, no swizzle
+  CUtensorMap tm_dk, tm_dv; // bf16 dK / dV [rows, Hkv, D], 32-row boxes (when kv_tma)
   const QTile* tiles;       // KV tiles (key rows in q_row0 / q_pos0 / q_rows / out_row0)
   const KvRun* runs;        // query runs
   const float* nl2;         // [H, ld]: -lse * log2(e) (-inf for a row with no key)
@@ -85,6 +86,7 @@ struct alignas(64) BwdParams {
   WsHeader* ws;
   int32_t n_tiles, H, Hkv;
   int32_t kv_group;         // KV heads per item group (divides Hkv)
+  int32_t kv_tma;           // 1: full 32-row slices of dK / dV leave through tm_dk / tm_dv
   float scale_log2;         // softmax scale * log2(e)
   float scale;              // softmax scale (dS is scaled by it)
 };
@@ -465,50 +467,103 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
       }
       const int64_t out_row = p.out_map ? p.out_map[tile.out_row0 + (key_ok ? row : 0)]
                                         : (int64_t)tile.out_row0 + row;
+      bool acc_read = false;
+      if (!kAccum && p.kv_tma && n > 0 && quad * 32 + 32 <= tile.q_rows) {
+        // All 32 key rows of this warp are valid: dV, then dK, leave through a
+        // tensor store each, staged in the warp's 8 KB share of the two dS^T
+        // buffers, which are free once the item's last dQ^T has run (Y's
+        // MMAs complete in issue order).
+        if (!__all_sync(0xffffffffu, wait_bounded(qd_empty + ((g - 1) & 1), ((g - 1) >> 1) & 1, abort_flag, p.ws, 20)))
+          break;
+        uint8_t* stg = smem + C::OFF_DS + quad * 8192;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        void* base = which ? p.dk : p.dv;
-        const uint32_t tcol = which ? C::TM_DK : C::TM_DV;
-#pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t v[32];
-          if (n > 0) {
-            tmem_ld32_wait(tl + tcol + 32u * cb, v);
-          } else {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = 0u;
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t tcol = which ? C::TM_DK : C::TM_DV;
+          if (which == 1) {
+            // dV's stores must have read the slice first
+            if (lane == 0) bulk_wait_group_read<0>();
+            __syncwarp();
           }
-          if (!key_ok) continue;
-          if (kAccum) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + (out_row * p.Hkv + it.g) * D + 32 * cb);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              float4 a = dst[q];
-              a.x += __uint_as_float(v[4 * q]);
-              a.y += __uint_as_float(v[4 * q + 1]);
-              a.z += __uint_as_float(v[4 * q + 2]);
-              a.w += __uint_as_float(v[4 * q + 3]);
-              dst[q] = a;
+          for (int hf = 0; hf < D / 64; ++hf) {
+            uint32_t v[64];
+            tmem_ld64_wait(tl + tcol + 64u * hf, v);
+            if (which == 1 && hf == D / 64 - 1) {
+              // dK and dV have been read: the next item's first dV / dK may overwrite them
+              tc_fence_before();
+              mbar_arrive(acc_free);
+              acc_read = true;
             }
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + (out_row * p.Hkv + it.g) * D +
-                                                  32 * cb);
+            const uint32_t row_addr = smem_u32(stg + hf * 4096) + lane * 128;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              dst[q] = make_uint4(
-                  pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                  pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                  pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                  pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+            for (int c = 0; c < 8; ++c)  // 16-byte chunk c of the row, 128-byte swizzle
+              st_shared_v4(row_addr + ((c ^ (lane & 7)) << 4),
+                           pack_bf16x2(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1])),
+                           pack_bf16x2(__uint_as_float(v[8 * c + 2]), __uint_as_float(v[8 * c + 3])),
+                           pack_bf16x2(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5])),
+                           pack_bf16x2(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int hf = 0; hf < D / 64; ++hf)
+              tma_store_3d(which ? &p.tm_dk : &p.tm_dv, stg + hf * 4096, 64 * hf, it.g, (int)out_row);
+            bulk_commit_group();
+          }
+        }
+        // the next item's dS^T copies may overwrite the slice once the stores have read it
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+      } else {
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          void* base = which ? p.dk : p.dv;
+          const uint32_t tcol = which ? C::TM_DK : C::TM_DV;
+#pragma unroll
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t v[32];
+            if (n > 0) {
+              tmem_ld32_wait(tl + tcol + 32u * cb, v);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 32; ++q) v[q] = 0u;
+            }
+            if (!key_ok) continue;
+            if (kAccum) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(base) + (out_row * p.Hkv + it.g) * D + 32 * cb);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                float4 a = dst[q];
+                a.x += __uint_as_float(v[4 * q]);
+                a.y += __uint_as_float(v[4 * q + 1]);
+                a.z += __uint_as_float(v[4 * q + 2]);
+                a.w += __uint_as_float(v[4 * q + 3]);
+                dst[q] = a;
+              }
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + (out_row * p.Hkv + it.g) * D +
+                                                    32 * cb);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                dst[q] = make_uint4(
+                    pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                    pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                    pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                    pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+            }
           }
         }
       }
       if (n > 0) {
-        tc_fence_before();
-        mbar_arrive(acc_free);
+        if (!acc_read) {
+          tc_fence_before();
+          mbar_arrive(acc_free);
+        }
         ++ac;
       }
     }
+    if (lane == 0) bulk_wait_group_all();  // this warp's tensor stores of dK / dV have completed
   } else if (warp < 10) {
     // ------------------------------------------------------------ dQ (one head-dim column per thread)
     const int quad = warp & 3;
@@ -768,6 +823,13 @@ cudaError_t launch_attn_bwd_bf16_tc(const BwdArgs& a, std::string* err) {
       !make_tensor_map_bf16(&p.tm_do, a.dout_rows, a.rows_total, a.H, a.D, 64, err) ||
       !make_tensor_map_f32(&p.tm_dq, a.dq_acc, a.rows_total, a.H, a.D, 64, err))
     return cudaErrorInvalidValue;
+  if (!a.accumulate && !a.out_map) {
+    // bf16 gradients at contiguous rows: full 32-row slices leave by tensor stores
+    if (!make_tensor_map_bf16(&p.tm_dk, a.dk, a.rows_total, a.Hkv, a.D, 32, err) ||
+        !make_tensor_map_bf16(&p.tm_dv, a.dv, a.rows_total, a.Hkv, a.D, 32, err))
+      return cudaErrorInvalidValue;
+    p.kv_tma = 1;
+  }
   p.tiles = a.tiles;
   p.runs = a.runs;
   p.nl2 = a.nl2;
