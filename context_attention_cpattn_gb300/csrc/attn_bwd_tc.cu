@@ -17,10 +17,14 @@
 // fp32 reductions into a global accumulator.
 //
 // Persistent blocks, one per SM (all 512 TMEM columns):
-//   TMEM  S^T[2] (2 x 64) | dP^T (64) | dQ^T (64) | dV (128) | dK (128)
+//   TMEM  S^T[2] (2 x 64) | dP^T[2] (2 x 64) | dV (128) | dK (128)
+//         dP^T buffer j & 1 holds dP^T_j, then dS^T_j (bf16, first 32
+//         columns), then dQ^T_j: Y issues dQ^T_j after dK_j, and one
+//         thread's MMAs run in issue order.
 // Warp roles (352 threads):
 //   warp 0      producer: K and V per item, Q_j and dO_j per piece through a
-//               two-deep ring (TMA), and the piece's -lse*log2(e) and -delta
+//               two-deep ring (TMA; a stage is refilled once dK_j, its last
+//               reader, has run), and the piece's -lse*log2(e) and -delta
 //               (plain loads by the 32 lanes) into shared memory.
 //   warp 1      TMEM allocator and MMA issuer X (one thread), per piece j:
 //                 S^T_j  = K Q_j^T   (M=128 keys, N=64, K=D)        SS
@@ -33,8 +37,8 @@
 //               shared memory faster than about one per 96 cycles, well under
 //               the tensor pipe's rate; two issuing threads keep twice as many
 //               in flight.  X reuses S buffer j & 1 once Y's dV_{j-2} has read
-//               P^T_{j-2}, and the dP^T buffer once Y's dK_{j-1} has read
-//               dS^T_{j-1} (mbarriers committed by Y).
+//               P^T_{j-2}, and dP^T buffer j & 1 once the dQ warps have read
+//               dQ^T_{j-2}.
 //   warps 2-5   one key per thread: P^T from S^T (exp2 with the saved LSE,
 //               causal mask from token positions), written back to TMEM as
 //               bf16; dS^T from dP^T, written to TMEM (for dK) and to shared
@@ -111,7 +115,8 @@ struct BwdCfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + 512;         // 36 mbarriers (288 bytes) below
   static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;      // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 192, TM_DV = 256, TM_DK = 384;
+  // S^T[2] | dP^T[2] (dP^T_j, then dS^T_j over its first 32 columns, then dQ^T_j) | dV | dK
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
 };
 
 // Walks the query runs of an item in pieces of up to 64 queries, once per
@@ -167,13 +172,11 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
   uint64_t* qd_full = bars + 2;    // [2] Q_j and dO_j landed
-  uint64_t* qd_empty = bars + 4;   // [2] every MMA of piece j has run (stage and dS^T buffer free)
+  uint64_t* qd_empty = bars + 4;   // [2] dK_j, the last MMA that reads stage j & 1, has run
   uint64_t* ld_full = bars + 6;    // [2] -lse2 / -delta of piece j in shared memory
   uint64_t* s_full = bars + 8;     // [2]
   uint64_t* p_full = bars + 10;    // [2]
-  uint64_t* dp_full = bars + 12;
   uint64_t* ds_full = bars + 13;
-  uint64_t* dq_free = bars + 15;
   uint64_t* acc_done = bars + 16;  // the item's last dK / dV MMA has run
   uint64_t* acc_free = bars + 17;  // the epilogue has read dK / dV
   uint64_t* drain = bars + 18;
@@ -182,7 +185,9 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
   uint64_t* stage_full = bars + 27;  // [2] the dQ staging tile is written
   uint64_t* stage_free = bars + 29;  // [2] its previous reduce has read it
   uint64_t* s_free = bars + 31;      // [2] dV_j has read P^T_j: S buffer j & 1 may be overwritten
-  uint64_t* dp_free = bars + 33;     // dK_j has read dS^T_j: the dP^T buffer may be overwritten
+  uint64_t* dp_full = bars + 36;     // [2] dP^T_j has run
+  uint64_t* dq_free = bars + 38;     // [2] the dQ warps have read dQ^T_j: dP^T buffer j & 1 is free
+  uint64_t* dq_ready = bars + 40;    // [2] dQ^T_j, piece j's last MMA, has run (its dS^T buffer is free)
   uint64_t* drain_y = bars + 34;
   uint64_t* ds_smem_full = bars + 35;  // dS^T_j's shared-memory copy (B of dQ^T) is written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -205,16 +210,18 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
       mbar_init(s_full + b, 1);
       mbar_init(p_full + b, 128);
     }
-    mbar_init(dp_full, 1);
     mbar_init(ds_full, 128);
-    mbar_init(dq_free, 128);
     mbar_init(acc_done, 1);
     mbar_init(acc_free, 128);
     mbar_init(drain, 1);
     mbar_init(drain_y, 1);
     mbar_init(s_free, 1);
     mbar_init(s_free + 1, 1);
-    mbar_init(dp_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(dp_full + b, 1);
+      mbar_init(dq_free + b, 128);
+      mbar_init(dq_ready + b, 1);
+    }
     mbar_init(ds_smem_full, 128);
     for (int r = 0; r < 4; ++r) {
       mbar_init(item_full + r, 1);
@@ -351,11 +358,12 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
           tc_fence_after();
           issue_t(tmem + C::TM_S + 64u * b, sK, sQ + b * C::QT_BYTES);
           umma_commit(s_full + b);
-          if (g >= 1) ok = wait_bounded(dp_free, (g - 1) & 1, abort_flag, p.ws, 23);
+          // dP^T buffer b last held dQ^T_{g-2}: the dQ warps must have read it
+          if (g >= 2) ok = wait_bounded(dq_free + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 23);
           if (!ok) break;
           tc_fence_after();
-          issue_t(tmem + C::TM_DP, sV, sDO + b * C::QT_BYTES);
-          umma_commit(dp_full);
+          issue_t(tmem + C::TM_DP + 64u * b, sV, sDO + b * C::QT_BYTES);
+          umma_commit(dp_full + b);
         }
       }
       umma_commit(drain);
@@ -423,7 +431,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
         tc_fence_before();
         mbar_arrive(p_full + b);
 
-        if (!__all_sync(0xffffffffu, wait_bounded(dp_full, g & 1, abort_flag, p.ws, 16))) {
+        if (!__all_sync(0xffffffffu, wait_bounded(dp_full + b, (g >> 1) & 1, abort_flag, p.ws, 16))) {
           ok = false;
           break;
         }
@@ -431,7 +439,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
         uint32_t ds[32];
         {
           uint32_t dr[64];
-          tmem_ld64_wait(tl + C::TM_DP, dr);
+          tmem_ld64_wait(tl + C::TM_DP + 64u * b, dr);
 #pragma unroll
           for (int q = 0; q < 32; ++q) {
             const float a0 = P[2 * q] * p.scale * (__uint_as_float(dr[2 * q]) + nd[2 * q]);
@@ -439,13 +447,13 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
             ds[q] = pack_bf16x2(a0, a1);
           }
         }
-        tmem_st32(tl + C::TM_DP, ds);  // dS^T (A of dK) over the first 32 columns of dP^T
+        tmem_st32(tl + C::TM_DP + 64u * b, ds);  // dS^T (A of dK) over the first 32 columns of dP^T
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(ds_full);  // dK_j may start; dQ^T_j waits for the copy below
         // dS^T for dQ^T: this buffer was last read by the dQ^T MMA of piece g - 2
         if (g >= 2 &&
-            !__all_sync(0xffffffffu, wait_bounded(qd_empty + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 17))) {
+            !__all_sync(0xffffffffu, wait_bounded(dq_ready + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 17))) {
           ok = false;
           break;
         }
@@ -473,7 +481,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
         // tensor store each, staged in the warp's 8 KB share of the two dS^T
         // buffers, which are free once the item's last dQ^T has run (Y's
         // MMAs complete in issue order).
-        if (!__all_sync(0xffffffffu, wait_bounded(qd_empty + ((g - 1) & 1), ((g - 1) >> 1) & 1, abort_flag, p.ws, 20)))
+        if (!__all_sync(0xffffffffu, wait_bounded(dq_ready + ((g - 1) & 1), ((g - 1) >> 1) & 1, abort_flag, p.ws, 20)))
           break;
         uint8_t* stg = smem + C::OFF_DS + quad * 8192;
 #pragma unroll
@@ -585,15 +593,15 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
         const Piece pc = cur.next(p.runs);
         const int sb = g & 1;
         // every MMA of piece g, dQ^T_g the last, has run
-        if (!__all_sync(0xffffffffu, wait_bounded(qd_empty + (g & 1), (g >> 1) & 1, abort_flag, p.ws, 20))) {
+        if (!__all_sync(0xffffffffu, wait_bounded(dq_ready + (g & 1), (g >> 1) & 1, abort_flag, p.ws, 20))) {
           ok = false;
           break;
         }
         tc_fence_after();
         uint32_t v[64];
-        tmem_ld64_wait(tl + C::TM_DQ, v);
+        tmem_ld64_wait(tl + C::TM_DP + 64u * sb, v);
         tc_fence_before();
-        mbar_arrive(dq_free);
+        mbar_arrive(dq_free + sb);
         // staging buffer sb: the reduce of piece g - 2 must have read it
         if (leader) {
           bulk_wait_group_read<1>();
@@ -655,19 +663,18 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)  // dK += dS^T Q
-            umma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + 8 * kk, smem_desc_sw128(qb + kk * 2048, C::QBOX, 1024),
+            umma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + 64u * b + 8 * kk, smem_desc_sw128(qb + kk * 2048, C::QBOX, 1024),
                          IDESC_KV, (t > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(dp_free);
-          if (g > 0) ok = wait_bounded(dq_free, (g - 1) & 1, abort_flag, p.ws, 12);
-          if (ok) ok = wait_bounded(ds_smem_full, g & 1, abort_flag, p.ws, 25);
+          umma_commit(qd_empty + b);  // stage b (Q_g, dO_g) may be refilled
+          ok = wait_bounded(ds_smem_full, g & 1, abort_flag, p.ws, 25);
           if (!ok) break;
           tc_fence_after();
           const uint32_t dsb = sDS + b * C::DS_BYTES;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dQ^T = K^T dS^T: 16 keys per MMA
-            umma_bf16_ss(tmem + C::TM_DQ, smem_desc_sw128(sK + kk * 2048, C::KBOX, 1024),
+            umma_bf16_ss(tmem + C::TM_DP + 64u * b, smem_desc_sw128(sK + kk * 2048, C::KBOX, 1024),
                          smem_desc_sw128(dsb + kk * 2048, C::DS_BYTES, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
-          umma_commit(qd_empty + b);  // also tells the dQ warps that dQ^T_g is ready
+          umma_commit(dq_ready + b);  // the dQ warps may read dQ^T_g; dS^T buffer b is free
           if (t == n - 1) {
             umma_commit(acc_done);
             umma_commit(kv_empty);
