@@ -112,7 +112,7 @@ struct BwdCfg {
   static constexpr uint32_t DQS_BYTES = 64 * D * 4;          // dQ staging tile (fp32)
   static constexpr uint32_t OFF_DQS = OFF_LD + 1024;          // dQ staging [2]
   static constexpr uint32_t OFF_BAR = OFF_DQS + 2 * DQS_BYTES;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + 512;         // 36 mbarriers (288 bytes) below
+  static constexpr uint32_t OFF_MISC = OFF_BAR + 512;         // 46 mbarriers (368 bytes) below
   static constexpr uint32_t SMEM = OFF_MISC + 64 + 1024;      // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   // S^T[2] | dP^T[2] (dP^T_j, then dS^T_j over its first 32 columns, then dQ^T_j) | dV | dK
@@ -176,7 +176,6 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
   uint64_t* ld_full = bars + 6;    // [2] -lse2 / -delta of piece j in shared memory
   uint64_t* s_full = bars + 8;     // [2]
   uint64_t* p_full = bars + 10;    // [2]
-  uint64_t* ds_full = bars + 13;
   uint64_t* acc_done = bars + 16;  // the item's last dK / dV MMA has run
   uint64_t* acc_free = bars + 17;  // the epilogue has read dK / dV
   uint64_t* drain = bars + 18;
@@ -188,8 +187,12 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
   uint64_t* dp_full = bars + 36;     // [2] dP^T_j has run
   uint64_t* dq_free = bars + 38;     // [2] the dQ warps have read dQ^T_j: dP^T buffer j & 1 is free
   uint64_t* dq_ready = bars + 40;    // [2] dQ^T_j, piece j's last MMA, has run (its dS^T buffer is free)
+  // dS^T_j written to TMEM (dK_j may start) and to shared memory (dQ^T_j may
+  // start), one barrier per piece parity: a softmax warp may run a piece
+  // ahead of the others, so consecutive pieces cannot share a barrier's phases
+  uint64_t* ds_full = bars + 42;       // [2]
+  uint64_t* ds_smem_full = bars + 44;  // [2]
   uint64_t* drain_y = bars + 34;
-  uint64_t* ds_smem_full = bars + 35;  // dS^T_j's shared-memory copy (B of dQ^T) is written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   int* issued = reinterpret_cast<int*>(smem + C::OFF_MISC + 16);     // loads issued: [0] K/V, [1] Q/dO
@@ -210,7 +213,10 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
       mbar_init(s_full + b, 1);
       mbar_init(p_full + b, 128);
     }
-    mbar_init(ds_full, 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(ds_full + b, 128);
+      mbar_init(ds_smem_full + b, 128);
+    }
     mbar_init(acc_done, 1);
     mbar_init(acc_free, 128);
     mbar_init(drain, 1);
@@ -222,7 +228,6 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
       mbar_init(dq_free + b, 128);
       mbar_init(dq_ready + b, 1);
     }
-    mbar_init(ds_smem_full, 128);
     for (int r = 0; r < 4; ++r) {
       mbar_init(item_full + r, 1);
       mbar_init(item_empty + r, 258);  // two MMA threads + 128 softmax + 128 dQ threads
@@ -450,7 +455,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
         tmem_st32(tl + C::TM_DP + 64u * b, ds);  // dS^T (A of dK) over the first 32 columns of dP^T
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(ds_full);  // dK_j may start; dQ^T_j waits for the copy below
+        mbar_arrive(ds_full + b);  // dK_j may start; dQ^T_j waits for the copy below
         // dS^T for dQ^T: this buffer was last read by the dQ^T MMA of piece g - 2
         if (g >= 2 &&
             !__all_sync(0xffffffffu, wait_bounded(dq_ready + b, ((g >> 1) - 1) & 1, abort_flag, p.ws, 17))) {
@@ -464,7 +469,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
             st_shared_v4(rbase + ((c ^ (row & 7)) << 4), ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
         }
         fence_proxy_async_smem();
-        mbar_arrive(ds_smem_full);
+        mbar_arrive(ds_smem_full + b);
       }
       if (!ok) break;
 
@@ -478,12 +483,13 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
       bool acc_read = false;
       if (!kAccum && p.kv_tma && n > 0 && quad * 32 + 32 <= tile.q_rows) {
         // All 32 key rows of this warp are valid: dV, then dK, leave through a
-        // tensor store each, staged in the warp's 8 KB share of the two dS^T
-        // buffers, which are free once the item's last dQ^T has run (Y's
-        // MMAs complete in issue order).
+        // tensor store each, staged in the warp's own rows of the two dS^T
+        // buffers (64 columns in each), which are free once the item's last
+        // dQ^T has run (Y's MMAs complete in issue order) and which no other
+        // warp writes.
         if (!__all_sync(0xffffffffu, wait_bounded(dq_ready + ((g - 1) & 1), ((g - 1) >> 1) & 1, abort_flag, p.ws, 20)))
           break;
-        uint8_t* stg = smem + C::OFF_DS + quad * 8192;
+        uint8_t* stg = smem + C::OFF_DS + quad * 4096;  // + hf * DS_BYTES: the rows in buffer hf
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           const uint32_t tcol = which ? C::TM_DK : C::TM_DV;
@@ -502,7 +508,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
               mbar_arrive(acc_free);
               acc_read = true;
             }
-            const uint32_t row_addr = smem_u32(stg + hf * 4096) + lane * 128;
+            const uint32_t row_addr = smem_u32(stg + hf * C::DS_BYTES) + lane * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c)  // 16-byte chunk c of the row, 128-byte swizzle
               st_shared_v4(row_addr + ((c ^ (lane & 7)) << 4),
@@ -516,7 +522,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
           if (lane == 0) {
 #pragma unroll
             for (int hf = 0; hf < D / 64; ++hf)
-              tma_store_3d(which ? &p.tm_dk : &p.tm_dv, stg + hf * 4096, 64 * hf, it.g, (int)out_row);
+              tma_store_3d(which ? &p.tm_dk : &p.tm_dv, stg + hf * C::DS_BYTES, 64 * hf, it.g, (int)out_row);
             bulk_commit_group();
           }
         }
@@ -658,7 +664,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
             umma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + 64u * b + 8 * kk,
                          smem_desc_sw128(dob + kk * 2048, C::QBOX, 1024), IDESC_KV, (t > 0 || kk > 0) ? 1u : 0u);
           umma_commit(s_free + b);
-          ok = wait_bounded(ds_full, g & 1, abort_flag, p.ws, 11);
+          ok = wait_bounded(ds_full + b, (g >> 1) & 1, abort_flag, p.ws, 11);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -666,7 +672,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
             umma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + 64u * b + 8 * kk, smem_desc_sw128(qb + kk * 2048, C::QBOX, 1024),
                          IDESC_KV, (t > 0 || kk > 0) ? 1u : 0u);
           umma_commit(qd_empty + b);  // stage b (Q_g, dO_g) may be refilled
-          ok = wait_bounded(ds_smem_full, g & 1, abort_flag, p.ws, 25);
+          ok = wait_bounded(ds_smem_full + b, (g >> 1) & 1, abort_flag, p.ws, 25);
           if (!ok) break;
           tc_fence_after();
           const uint32_t dsb = sDS + b * C::DS_BYTES;
