@@ -10,11 +10,13 @@
 //     dV += P^T dO      dP = dO V^T      dS = P (dP - delta)
 //     dK += scale dS^T Q                  dQ += scale dS K
 //
-// A work item is one KV tile (128 keys of one sequence in one rank's shard)
-// of one KV head.  It walks, for each query head of the group, the query runs
+// A work item is one KV tile (up to 128 keys of one sequence: inside one
+// rank's chunk for a ring step, cut from the sequence for a whole call) of
+// one KV head.  It walks, for each query head of the group, the query runs
 // that see it in ring order, 64 queries at a time; dK and dV stay in TMEM for
 // the whole item and are written once, and each piece's dQ leaves through
-// fp32 reductions into a global accumulator.
+// fp32 reductions into a global accumulator.  Items run in groups of KV heads
+// (see item_of).
 //
 // Persistent blocks, one per SM (all 512 TMEM columns):
 //   TMEM  S^T[2] (2 x 64) | dP^T[2] (2 x 64) | dV (128) | dK (128)
@@ -43,7 +45,8 @@
 //               causal mask from token positions), written back to TMEM as
 //               bf16; dS^T from dP^T, written to TMEM (for dK) and to shared
 //               memory (the B operand of dQ^T); at the end of the item dK and
-//               dV from TMEM to global memory.
+//               dV from TMEM to global memory, staged in the warp's own rows of
+//               the two dS^T buffers and written by tensor stores.
 //   warps 6-9   one head-dim column per thread: read dQ^T_j from TMEM into a
 //               [64 queries][D] fp32 tile in shared memory (two buffers); one
 //               thread adds the tile to the fp32 dQ accumulator with a TMA

@@ -9,10 +9,11 @@
 // ring step's partial (O_t, lse_t) is folded in as soon as it is produced and
 // never leaves the SM.
 //
-// Persistent blocks, two per SM (about 101 KB of shared memory and 256 TMEM
-// columns each).  The producer warp hands out work items (the first by block
-// index, the rest from an atomic counter, longest first) through a ring of
-// shared-memory slots.
+// Persistent blocks, two per SM (113 KB of shared memory, 16 KB of it the
+// epilogue's staging area, and 256 TMEM columns each).  The producer warp
+// hands out work items (the first by block index, the rest from an atomic
+// counter) through a ring of shared-memory slots.  Items run in groups of KV
+// heads (see item_of), tile by tile longest first inside a group.
 //
 // Warp roles (224 threads):
 //   warp 0      TMA producer: Q per item, then K and V through two-deep
