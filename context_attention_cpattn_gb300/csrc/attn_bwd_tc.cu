@@ -25,8 +25,8 @@
 //         thread's MMAs run in issue order.
 // Warp roles (352 threads):
 //   warp 0      producer: K and V per item, Q_j and dO_j per piece through a
-//               two-deep ring (TMA; a stage is refilled once dK_j, its last
-//               reader, has run), and the piece's -lse*log2(e) and -delta
+//               ring of NSTAGE stages (TMA; a stage is refilled once dK_j,
+//               its last reader, has run), and the piece's -lse*log2(e) and -delta
 //               (plain loads by the 32 lanes) into shared memory.
 //   warp 1      TMEM allocator and MMA issuer X (one thread), per piece j:
 //                 S^T_j  = K Q_j^T   (M=128 keys, N=64, K=D)        SS
@@ -48,7 +48,7 @@
 //               dV from TMEM to global memory, staged in the warp's own rows of
 //               the two dS^T buffers and written by tensor stores.
 //   warps 6-9   one head-dim column per thread: read dQ^T_j from TMEM into a
-//               [64 queries][D] fp32 tile in shared memory (two buffers); one
+//               [64 queries][D] fp32 tile in shared memory (NDQ buffers); one
 //               thread adds the tile to the fp32 dQ accumulator with a TMA
 //               reduce-add (performed in L2).  Rows past the piece hold exact
 //               zeros (their dS is zero), so the whole 64-row box is added.
