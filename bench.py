@@ -374,7 +374,7 @@ def run_reference(args):
     w = inputs.workload(args.workload)
     q, k, v = inputs.make_qkv(w)
     cores = host_cores()
-    rows_per_step = args.rows or 96
+    rows_per_step = args.rows or w.T  # every row: K and V are converted to fp64 once per step either way
     times, fl_total = [], 0
     for i in range(args.warmup + args.steps):
         rows = inputs.sample_rows(w.T, rows_per_step, seed=w.seed + 100 + i)
@@ -892,8 +892,17 @@ def main(argv=None):
         return
     if args.impl == "reference":
         # host-only: rank 0 runs it, other ranks exit without work (no process group)
-        if int(os.environ.get("RANK", "0")) == 0:
-            run_reference(args)
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        if os.environ.get("OPENBLAS_NUM_THREADS") != "1":
+            # the oracle's thread pool supplies the parallelism: restart with
+            # single-threaded BLAS, as the cpu_baseline child does
+            env = dict(os.environ)
+            for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+                env[var] = "1"
+            sys.stdout.flush()
+            os.execve(sys.executable, [sys.executable, os.path.abspath(__file__)] + sys.argv[1:], env)
+        run_reference(args)
         return
     rep = Replicas()
     try:
