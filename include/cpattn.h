@@ -232,7 +232,10 @@ cpattn_status_t cpattn_plan_get_a2a_map(const cpattn_plan_t* plan, int64_t* out,
  *     sequence's last row, up to the kernel's tile height, so it may hold
  *     the end of one chunk and the start of the next; its rank owns its last
  *     row and its runs follow that rank's ring, with the position mask in
- *     every run that crosses the tile's first query.
+ *     every run that crosses the tile's first query.  A key tile of a whole
+ *     backward call on global rows is cut from its sequence's first row on;
+ *     its rank owns its first key and its query runs follow that rank's
+ *     ring.  Runs of one ring step that continue each other are merged.
  *   run: row0, pos0, len = rows of the other side; masked = 1 when the
  *     position mask (key position <= query position) applies inside the run,
  *     0 when every pair of the tile and the run is allowed.
