@@ -772,7 +772,10 @@ def run_aux(args):
     """GB/s of the HBM-bound kernels on shapes of the workloads: the exact LSE
     merge of cp=4 partials over the 32K micro-batch, the grid2d shard gather of
     the 16x45x80 latent's Q, and the loss normalisation (micro-batch size and
-    a 64M-token vector).  Algorithmic bytes: everything read once + written once."""
+    a 64M-token vector).  Algorithmic bytes: everything read once + written once.
+    Also: the host link, the ring written out as block steps and merges (the
+    micro-batch and the 200K-token sequence) against the fused forward, and
+    the Dynamic-CP solver's host time."""
     import torch
 
     import context_attention_cpattn_gb300 as cp
@@ -866,6 +869,8 @@ def run_aux(args):
         rec(f"H2D copy kernel, {blocks} blocks", timeit(lambda: cp.cpattn_copy(dbuf, hbuf, n_blocks=blocks), reps=5))
         rec(f"D2H copy kernel, {blocks} blocks", timeit(lambda: cp.cpattn_copy(hbuf, dbuf, n_blocks=blocks), reps=5))
     del hbuf, dbuf
+    ring = [materialised_ring(cp, inputs, dev, timeit),
+            materialised_ring(cp, inputs, dev, timeit, "long_video_200k_gqa", reps=2)]
     # Dynamic-CP solver (host C++): the micro-batch count sweep over a global
     # batch of 2048 long-tailed samples, dp 8, pp 4, V 2, m = 4..16
     rng = np.random.default_rng(3)
@@ -875,8 +880,67 @@ def run_aux(args):
         r = cp.cpattn_dcp_sweep(L, 8, 4, 2, 4, 8, 16384, 4 * 128 * 32, 0)
     host = [{"solver": "cpattn_dcp_sweep", "shape": "2048 samples, dp 8, pp 4, V 2, m 4..16 (13 schedules)",
              "ms": (time.perf_counter() - t0) / reps * 1e3, "knee_m": r["knee_m"], "best_m": r["best_m"]}]
-    print(json.dumps({"aux": out, "host_link": link, "host": host, "hbm_peak_GB_s": peak, "peak_source": src}),
-          flush=True)
+    print(json.dumps({"aux": out, "host_link": link, "ring": ring, "host": host, "hbm_peak_GB_s": peak,
+                      "peak_source": src}), flush=True)
+
+
+def materialised_ring(cp, inputs, dev, timeit, name="dynamic_cp_microbatch", reps=5):
+    """A workload's ring written out step by step: for each of the cp virtual
+    ranks, cp block attention steps (cpattn_block_fwd, fp32 partial O and LSE
+    per step) and one exact merge of the partials into the rank's rows; beside
+    it the fused forward (cpattn_fwd) on the same inputs.  The ring's steps
+    together cover every valid (query, key) pair once, so their FLOPs are the
+    forward's.  The ranks run one after another and share the partial
+    buffers; the block steps are also timed on their own."""
+    import torch
+
+    w = inputs.workload(name)
+    q_h, k_h, v_h = inputs.make_qkv(w)
+    qd, kd, vd = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    del q_h, k_h, v_h
+    plan = cp.cpattn_plan(w.cu_seqlens, w.cp, w.mode, w.grid)
+    ws = torch.empty(cp.cpattn_workspace_size(plan, w.H, w.Hkv, w.D, qd.dtype, w.causal), dtype=torch.uint8,
+                     device=dev)
+    ro = plan.rank_offsets()
+    idx = torch.from_numpy(plan.index_map()).to(dev)
+    rows = [int(ro[r + 1] - ro[r]) for r in range(w.cp)]
+    n_max = max(rows)
+    po_buf = [torch.empty(n_max * w.H * w.D, dtype=torch.float32, device=dev) for _ in range(w.cp)]
+    pl_buf = [torch.empty(w.H * n_max, dtype=torch.float32, device=dev) for _ in range(w.cp)]
+    po = [[b[:n * w.H * w.D].view(n, w.H, w.D) for b in po_buf] for n in rows]
+    pl = [[b[:w.H * n].view(w.H, n) for b in pl_buf] for n in rows]
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.H, w.T), dtype=torch.float32, device=dev)
+    flops = cp.cpattn_fwd_flops(w.cu_seqlens, w.H, w.D, w.causal)
+    peak, _ = measured_peak()
+
+    def steps(r):
+        for t in range(w.cp):
+            cp.cpattn_block_fwd(plan, qd, kd, vd, po[r][t], pl[r][t], ws, r, t, scale=w.scale, causal=w.causal)
+
+    def merge(r):
+        cp.cpattn_merge(po[r], pl[r], o, lse, out_rows=idx[int(ro[r]):int(ro[r + 1])])
+
+    def ring():
+        for r in range(w.cp):
+            steps(r)
+            merge(r)
+
+    def all_steps():
+        for r in range(w.cp):
+            steps(r)
+
+    def fused():
+        cp.cpattn_fwd(plan, qd, kd, vd, o, lse, ws, scale=w.scale, causal=w.causal)
+
+    res = {}
+    for key, fn in (("ring (steps + merges)", ring), ("block steps", all_steps), ("fused forward", fused)):
+        sec = timeit(fn, reps=reps)
+        tf = flops / sec / 1e12
+        res[key] = {"ms": sec * 1e3, "TFLOP/s": tf, "frac": tf / peak}
+    cp.cpattn_sync_status(ws)
+    return {"workload": w.name, "shape": f"cp={w.cp} ranks x {w.cp} steps, T={w.T}, H={w.H}, Hkv={w.Hkv}, D={w.D}",
+            "flops": flops, "launches": w.cp * (w.cp + 1), **res}
 
 
 def main(argv=None):
