@@ -551,7 +551,8 @@ def run_ours(args, rep: Replicas):
                B["res_h"].numel() * 8)
         e2e = {"value": rep.world * args.steps * flops / e2e_s / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "pipelined": True,
-               "ms_per_step": 1e3 * e2e_s / args.steps}
+               "ms_per_step": 1e3 * e2e_s / args.steps,
+               "host_link_GB_s": (h2d + d2h) * args.steps / e2e_s / 1e9}
         cp.cpattn_sync_status(ws, stream)
         # the read-back of the last step holds the same result as the device-timed steps
         if not torch.equal(sets[(args.warmup + args.steps - 1) % 2]["o_h"].to(dev), o):
@@ -868,7 +869,26 @@ def run_aux(args):
     for blocks in (38, 152, 608):
         rec(f"H2D copy kernel, {blocks} blocks", timeit(lambda: cp.cpattn_copy(dbuf, hbuf, n_blocks=blocks), reps=5))
         rec(f"D2H copy kernel, {blocks} blocks", timeit(lambda: cp.cpattn_copy(hbuf, dbuf, n_blocks=blocks), reps=5))
-    del hbuf, dbuf
+    # both directions at once, as the pipelined end-to-end step moves them: H2D of the
+    # 805 MB above beside D2H of 805 MB from a second pair of buffers (bytes = both)
+    hbuf2 = torch.empty(nb, dtype=torch.uint8, pin_memory=True)
+    dbuf2 = torch.empty(nb, dtype=torch.uint8, device=dev)
+
+    def both():
+        cur = torch.cuda.current_stream(dev)
+        for st in streams[:2]:
+            st.wait_stream(cur)
+        with torch.cuda.stream(streams[0]):
+            dbuf.copy_(hbuf, non_blocking=True)
+        with torch.cuda.stream(streams[1]):
+            hbuf2.copy_(dbuf2, non_blocking=True)
+        for st in streams[:2]:
+            cur.wait_stream(st)
+
+    sec = timeit(both, reps=5)
+    link.append({"what": "H2D and D2H at once, cudaMemcpyAsync on two streams", "bytes": 2 * nb, "ms": sec * 1e3,
+                 "GB_s": 2 * nb / sec / 1e9})
+    del hbuf, dbuf, hbuf2, dbuf2
     ring = [materialised_ring(cp, inputs, dev, timeit),
             materialised_ring(cp, inputs, dev, timeit, "long_video_200k_gqa", reps=2)]
     # Dynamic-CP solver (host C++): the micro-batch count sweep over a global
