@@ -26,7 +26,7 @@
 // Warp roles (352 threads):
 //   warp 0      producer: K and V per item, Q_j and dO_j per piece through a
 //               ring of NSTAGE stages (TMA; a stage is refilled once dK_j,
-//               its last reader, has run), and the piece's -lse*log2(e) and -delta
+//               its last reader, has run), and the piece's -lse*log2(e) and -scale*delta
 //               (plain loads by the 32 lanes) into shared memory.
 //   warp 1      TMEM allocator and MMA issuer X (one thread), per piece j:
 //                 S^T_j  = K Q_j^T   (M=128 keys, N=64, K=D)        SS
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
   uint64_t* kv_empty = bars + 1;
   uint64_t* qd_full = bars + 2;    // [NST] Q_j and dO_j landed
   uint64_t* qd_empty = bars + 5;   // [NST] dK_j, the last MMA that reads stage j % NST, has run
-  uint64_t* ld_full = bars + 8;    // [NST] -lse2 / -delta of piece j in shared memory
+  uint64_t* ld_full = bars + 8;    // [NST] -lse2 / -scale*delta of piece j in shared memory
   uint64_t* s_full = bars + 11;    // [2]
   uint64_t* p_full = bars + 13;    // [2]
   uint64_t* acc_done = bars + 15;  // the item's last dK / dV MMA has run
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
           }
           issued[1] = g + 1;
         }
-        // the piece's -lse*log2(e) and -delta (columns past the piece: -inf and 0, so P = 0 there)
+        // the piece's -lse*log2(e) and -scale*delta (columns past the piece: -inf and 0, so P = 0 there)
         float* dst = ldv + st * 128;
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
           const bool in = c < pc.len;
           const int64_t src = (int64_t)h * p.ld + pc.row0 + (in ? c : 0);
           dst[c] = in ? p.nl2[src] : -INFINITY;
-          dst[64 + c] = in ? p.nd[src] : 0.f;
+          dst[64 + c] = in ? p.nd[src] * p.scale : 0.f;
         }
         mbar_arrive(ld_full + st);
       }
@@ -455,11 +455,14 @@ __global__ void __launch_bounds__(352, 1) attn_bwd_tc_kernel(const __grid_consta
         {
           uint32_t dr[64];
           tmem_ld64_wait(tl + C::TM_DP + 64u * b, dr);
+          // dS = P * (scale * dP - scale * delta), two queries per packed FMA and multiply
+          const float2 sc2 = make_float2(p.scale, p.scale);
 #pragma unroll
           for (int q = 0; q < 32; ++q) {
-            const float a0 = P[2 * q] * p.scale * (__uint_as_float(dr[2 * q]) + nd[2 * q]);
-            const float a1 = P[2 * q + 1] * p.scale * (__uint_as_float(dr[2 * q + 1]) + nd[2 * q + 1]);
-            ds[q] = pack_bf16x2(a0, a1);
+            const float2 t = __ffma2_rn(make_float2(__uint_as_float(dr[2 * q]), __uint_as_float(dr[2 * q + 1])), sc2,
+                                        make_float2(nd[2 * q], nd[2 * q + 1]));
+            const float2 a = __fmul2_rn(make_float2(P[2 * q], P[2 * q + 1]), t);
+            ds[q] = pack_bf16x2(a.x, a.y);
           }
         }
         tmem_st32(tl + C::TM_DP + 64u * b, ds);  // dS^T (A of dK) over the first 32 columns of dP^T
