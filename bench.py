@@ -595,6 +595,7 @@ def run_ours(args, rep: Replicas):
         "tc_source_sha256": tc_source_hash(),
         "mma_area_useful": useful_mma_fraction(plan, w.causal, w.dtype),
     }
+    add_sustained(line["roofline"], achieved, clocks)
     if per_config is not None:
         line["per_config"] = per_config
     if backward is not None:
@@ -616,6 +617,16 @@ def measured_sustained() -> float | None:
             return float(json.load(f)["bf16_tflops_sustained"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+def add_sustained(roofline: dict, achieved: float, clocks) -> None:
+    """When the power cap held the clocks down during the timed region, the
+    fraction of the measured sustained bf16 peak (a long loop under the same
+    cap) goes beside the fraction of the burst peak."""
+    sustained = measured_sustained()
+    if sustained and clocks and "sw_power_cap" in clocks.get("reasons", []):
+        roofline["frac_of_sustained"] = achieved / sustained
+        roofline["peak_sustained"] = sustained
 
 
 def time_config(cp, name, steps, dev, stream, sampler, warmup=3):
@@ -730,7 +741,8 @@ def time_backward(cp, w, qd, kd, vd, dev, stream, sampler, steps, warmup, tag="b
     peak, peak_src = measured_peak()
     achieved = flops / mean_s / 1e12
     launches = 3 + (4 if w.mode == "grid2d" else 0)
-    return {
+    clocks = sampler.summary(tag, tag + "_end")
+    out = {
         "metric": "packed varlen attention bwd TFLOP/s (valid tokens, 2.5x forward FLOPs)", "value": achieved,
         "unit": UNIT, "steps": steps, "warmup": warmup, "ms_per_step": 1e3 * mean_s,
         "ms_min": min(ms), "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
@@ -739,8 +751,10 @@ def time_backward(cp, w, qd, kd, vd, dev, stream, sampler, steps, warmup, tag="b
                      "peak_source": peak_src,
                      "traffic": recorded_traffic(w.name, "attn_bwd_tc_kernel", BWD_SOURCES),
                      "kernel": "cpattn_bwd call (pre + attn_bwd_tc_kernel + post), CUDA events per call"},
-        "gpu_launches": launches * steps, "clocks": sampler.summary(tag, tag + "_end"),
+        "gpu_launches": launches * steps, "clocks": clocks,
         "mma_area_useful": useful_mma_fraction(plan, w.causal, w.dtype, backward=True)}
+    add_sustained(out["roofline"], achieved, clocks)
+    return out
 
 
 def run_bwd(args):

@@ -90,3 +90,14 @@ def test_useful_mma_area_of_the_workloads(cpattn):
     assert 0.96 < bench.useful_mma_fraction(one, True) < 0.98
     full = cpattn.cpattn_plan([0, 4096], 2, "zigzag")
     assert bench.useful_mma_fraction(full, False) == 1.0
+
+
+def test_sustained_fraction_only_under_the_power_cap(monkeypatch):
+    monkeypatch.setattr(bench, "measured_sustained", lambda: 1700.0)
+    capped = {}
+    bench.add_sustained(capped, 850.0, {"reasons": ["sw_power_cap"], "sm_mhz": 1777.0})
+    assert capped == {"frac_of_sustained": 0.5, "peak_sustained": 1700.0}
+    free = {}
+    bench.add_sustained(free, 850.0, {"reasons": [], "sm_mhz": 2070.0})
+    bench.add_sustained(free, 850.0, None)
+    assert free == {}
